@@ -1,0 +1,324 @@
+"""Seeded synthetic All-Gather rounds: the inputs both the CUDA path and the oracle consume.
+
+This module draws random numbers and integer placements only. It holds none of the
+method's arithmetic (no rotation, no deviation, no selection, no diffing): a caller that
+needs a "freshly recomputed" K builds it from the reused K it already has plus the noise
+drawn here.
+
+Workload shape (TokenDance, "Summary — Motivation" and Figure 1): agent i's prompt is its
+private history H_i followed by the N shared output blocks in an agent-specific order
+Pi_i. The pages measure on GenerativeAgents / AgentSociety traces with Qwen2.5-7B/14B;
+those traces and weights are not available, so the rounds below stand in for them with
+the model shapes (layers, KV heads, head_dim), the block and history lengths and the
+perturbation fractions of the five workloads this library is tested on.
+
+Random source: SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+generators", OOPSLA 2014), used counter-style: element n of a stream with key K is
+mix(K + (n+1)*GAMMA). Normals are an Irwin-Hall sum of four 16-bit uniforms, scaled to
+unit variance in float64 (exact integer sum, one IEEE division), so every machine draws
+identical bits.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+
+_U = np.uint64
+GAMMA = _U(0x9E3779B97F4A7C15)
+_M1 = _U(0xBF58476D1CE4E5B9)
+_M2 = _U(0x94D049BB133111EB)
+# Irwin-Hall(4) of uniform integers on [0, 65535]: mean 2*65535, variance 4*(65536^2-1)/12
+_IH_MEAN = 2 * 65535
+_IH_SD = math.sqrt(4.0 * (65536.0 * 65536.0 - 1.0) / 12.0)
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> _U(30))) * _M1
+    z = (z ^ (z >> _U(27))) * _M2
+    return z ^ (z >> _U(31))
+
+
+def _tag(s) -> int:
+    if isinstance(s, str):
+        h = 1469598103934665603  # FNV-1a over the tag's bytes
+        for ch in s.encode():
+            h = ((h ^ ch) * 1099511628211) & 0xFFFFFFFFFFFFFFFF
+        return h
+    return int(s) & 0xFFFFFFFFFFFFFFFF
+
+
+def stream_key(seed: int, *ids) -> np.uint64:
+    """Key of the sub-stream named by (seed, ids...)."""
+    k = _mix(np.array([_tag(seed)], dtype=_U) + GAMMA)
+    for x in ids:
+        k = _mix(k ^ _mix(np.array([_tag(x)], dtype=_U) + GAMMA))
+    return k[0]
+
+
+def uniform_u64(key, counters: np.ndarray) -> np.ndarray:
+    """SplitMix64 output for each counter (any integer array, >= 0)."""
+    c = np.asarray(counters, dtype=_U)
+    return _mix(_U(key) + (c + _U(1)) * GAMMA)
+
+
+def normal_f64(key, counters: np.ndarray) -> np.ndarray:
+    """Approximately N(0, 1) per counter: Irwin-Hall(4) of 16-bit uniforms, unit variance."""
+    u = uniform_u64(key, counters)
+    m = _U(0xFFFF)
+    s = (u & m) + ((u >> _U(16)) & m) + ((u >> _U(32)) & m) + (u >> _U(48))
+    return (s.astype(np.int64) - _IH_MEAN).astype(np.float64) / _IH_SD
+
+
+def randint(key, counters, lo: int, hi: int) -> np.ndarray:
+    """Integers uniform on [lo, hi] (inclusive)."""
+    span = _U(hi - lo + 1)
+    return (uniform_u64(key, counters) % span).astype(np.int64) + lo
+
+
+# ---------------------------------------------------------------- bf16 storage helpers
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit pattern (uint16), round to nearest even; NaN stays NaN."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    is_nan = (b & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+    r = (b + (np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1)))) >> np.uint32(16)
+    r = np.where(is_nan, (b >> np.uint32(16)) | np.uint32(0x40), r)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+# ---------------------------------------------------------------- workload descriptions
+@dataclasses.dataclass(frozen=True)
+class RoundConfig:
+    """One synthetic All-Gather round: model shape, placement and perturbation recipe."""
+
+    name: str
+    n_agents: int
+    n_layers: int
+    n_kv_heads: int
+    head_dim: int
+    page_size: int
+    block_lens: tuple                 # length of each shared output block, canonical order
+    hist_range: tuple                 # (lo, hi) inclusive, uniform; ignored if hist_fixed
+    hist_fixed: Optional[tuple] = None
+    check_layer: int = 1
+    recompute_pct: int = 15
+    perturb_mode: str = "runs"        # "runs": clustered runs of 1..64 tokens; "uniform"
+    perturb_frac: tuple = (0.10, 0.20)  # per-agent fraction, uniform on [lo, hi]
+    rope_theta: float = 1.0e6
+    diff_block: int = 16
+    pool_bytes: Optional[int] = None  # paged pool size; None = exactly the pages needed
+    seed: int = 1000
+
+    @property
+    def n_blocks(self) -> int:
+        return len(self.block_lens)
+
+    @property
+    def n_shared(self) -> int:
+        return int(sum(self.block_lens))
+
+    @property
+    def elems(self) -> int:
+        return self.n_kv_heads * self.head_dim
+
+    @property
+    def k_select(self) -> int:
+        return (self.recompute_pct * self.n_shared + 99) // 100
+
+    def replace(self, **kw) -> "RoundConfig":
+        return dataclasses.replace(self, **kw)
+
+
+def tiny() -> RoundConfig:
+    return RoundConfig(
+        name="tiny_n3_l2_h2x64_s96", n_agents=3, n_layers=2, n_kv_heads=2, head_dim=64,
+        page_size=16, block_lens=(32, 32, 32), hist_range=(0, 0), hist_fixed=(5, 17, 40),
+        check_layer=0, recompute_pct=15, perturb_mode="uniform", perturb_frac=(0.15, 0.15),
+        seed=1000)
+
+
+def qwen7b() -> RoundConfig:
+    return RoundConfig(
+        name="qwen2.5-7b_n10_l28_h4x128_s2560", n_agents=10, n_layers=28, n_kv_heads=4,
+        head_dim=128, page_size=16, block_lens=(256,) * 10, hist_range=(500, 4000),
+        check_layer=1, recompute_pct=15, seed=1001)
+
+
+def qwen14b() -> RoundConfig:
+    return RoundConfig(
+        name="qwen2.5-14b_n10_l48_h8x128_s5120", n_agents=10, n_layers=48, n_kv_heads=8,
+        head_dim=128, page_size=16, block_lens=(512,) * 10, hist_range=(1000, 8000),
+        check_layer=1, recompute_pct=15, seed=1002)
+
+
+def scale64() -> RoundConfig:
+    return RoundConfig(
+        name="qwen2.5-7b_n64_l28_h4x128_s8192", n_agents=64, n_layers=28, n_kv_heads=4,
+        head_dim=128, page_size=16, block_lens=(128,) * 64, hist_range=(0, 16384),
+        check_layer=1, recompute_pct=15, seed=1003)
+
+
+def density(pct: int, page_size: int = 16, pool_bytes: Optional[int] = 120 * 10**9) -> RoundConfig:
+    f = pct / 100.0
+    return RoundConfig(
+        name=f"qwen2.5-14b_n32_l48_h8x128_s16384_p{pct}_pg{page_size}", n_agents=32,
+        n_layers=48, n_kv_heads=8, head_dim=128, page_size=page_size,
+        block_lens=(512,) * 32, hist_range=(1000, 8000), check_layer=1, recompute_pct=pct,
+        perturb_frac=(f, f), pool_bytes=pool_bytes, seed=1004)
+
+
+CONFIGS = {"tiny": tiny, "qwen7b": qwen7b, "qwen14b": qwen14b, "scale64": scale64}
+
+
+# ---------------------------------------------------------------- the round itself
+@dataclasses.dataclass
+class Round:
+    cfg: RoundConfig
+    block_len: np.ndarray      # [M] int32
+    hist_len: np.ndarray       # [N] int32
+    perm: np.ndarray           # [N, M] int32: perm[i, q] = block at slot q of agent i
+    perturbed: np.ndarray      # [N, S] bool: tokens whose fresh K/V carry large noise
+    block_table: np.ndarray    # [N, max_lp] int32, -1 = unmapped
+    num_pages: int
+
+
+def _perturbed_mask(cfg: RoundConfig, seed: int) -> np.ndarray:
+    N, S = cfg.n_agents, cfg.n_shared
+    out = np.zeros((N, S), dtype=bool)
+    lo, hi = cfg.perturb_frac
+    for i in range(N):
+        cnt_lo = int(math.ceil(lo * S - 1e-9))
+        cnt_hi = int(math.floor(hi * S + 1e-9))
+        cnt_hi = max(cnt_hi, cnt_lo)
+        target = int(randint(stream_key(seed, "pert-count", i), [0], cnt_lo, cnt_hi)[0])
+        target = min(target, S)
+        if cfg.perturb_mode == "uniform":
+            keys = uniform_u64(stream_key(seed, "pert-uniform", i), np.arange(S))
+            out[i, np.argsort(keys, kind="stable")[:target]] = True
+            continue
+        key = stream_key(seed, "pert-runs", i)
+        marked, n = 0, 0
+        while marked < target:
+            r = uniform_u64(key, [n])[0]
+            n += 1
+            run = int(r % _U(64)) + 1
+            start = int((r >> _U(8)) % _U(max(S - run + 1, 1)))
+            for t in range(start, min(start + run, S)):
+                if not out[i, t]:
+                    out[i, t] = True
+                    marked += 1
+                    if marked == target:
+                        break
+    return out
+
+
+def make_round(cfg: RoundConfig, seed: Optional[int] = None,
+               map_history: bool = False) -> Round:
+    """Round descriptor, perturbation mask and a randomly permuted page table.
+
+    Pages that hold only private history stay unmapped (-1) unless map_history.
+    """
+    seed = cfg.seed if seed is None else seed
+    N, M, S, P = cfg.n_agents, cfg.n_blocks, cfg.n_shared, cfg.page_size
+    block_len = np.asarray(cfg.block_lens, dtype=np.int32)
+    if cfg.hist_fixed is not None:
+        hist = np.asarray(cfg.hist_fixed, dtype=np.int32)
+    else:
+        hist = randint(stream_key(seed, "hist"), np.arange(N), *cfg.hist_range).astype(np.int32)
+    perm = np.empty((N, M), dtype=np.int32)
+    for i in range(N):
+        keys = uniform_u64(stream_key(seed, "perm", i), np.arange(M))
+        perm[i] = np.argsort(keys, kind="stable")
+    perturbed = _perturbed_mask(cfg, seed)
+
+    max_lp = int(max((int(h) + S + P - 1) // P for h in hist))
+    first = [0 if map_history else int(h) // P for h in hist]
+    last = [(int(h) + S - 1) // P for h in hist]
+    need = sum(l - f + 1 for f, l in zip(first, last))
+    page_bytes = cfg.n_layers * 2 * P * cfg.elems * 2
+    num_pages = need if cfg.pool_bytes is None else max(need, cfg.pool_bytes // page_bytes)
+    phys = np.argsort(uniform_u64(stream_key(seed, "pages"), np.arange(num_pages)),
+                      kind="stable").astype(np.int32)
+    bt = np.full((N, max_lp), -1, dtype=np.int32)
+    c = 0
+    for i in range(N):
+        n_i = last[i] - first[i] + 1
+        bt[i, first[i]:last[i] + 1] = phys[c:c + n_i]
+        c += n_i
+    return Round(cfg, block_len, hist, perm, perturbed, bt, int(num_pages))
+
+
+# ---------------------------------------------------------------- tensors
+def canonical_kv(cfg: RoundConfig, seed: Optional[int] = None, layers=None,
+                 chunk_rows: int = 4096):
+    """Canonical-frame K and V, [L][S][E] bf16 bits (uint16), entries ~ N(0, 1)."""
+    seed = cfg.seed if seed is None else seed
+    L, S, E = cfg.n_layers, cfg.n_shared, cfg.elems
+    layers = range(L) if layers is None else layers
+    out = []
+    for kv in ("K", "V"):
+        arr = np.empty((len(layers), S, E), dtype=np.uint16)
+        for li, l in enumerate(layers):
+            key = stream_key(seed, "canon", kv, l)
+            for t0 in range(0, S, chunk_rows):
+                t1 = min(S, t0 + chunk_rows)
+                ctr = np.arange(t0 * E, t1 * E, dtype=np.uint64)
+                arr[li, t0:t1] = f32_to_bf16_bits(
+                    normal_f64(key, ctr).astype(np.float32)).reshape(t1 - t0, E)
+        out.append(arr)
+    return out[0], out[1]
+
+
+def _noise_rows(seed, tag, agent, layer, tokens, perturbed_rows, E):
+    """Noise for whole token rows: N(0, 1e-3) everywhere plus N(0, 0.5) on perturbed rows."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    pr = np.asarray(perturbed_rows, dtype=bool)
+    lane = np.arange(E, dtype=np.int64)[None, :]
+    ctr = (tokens[:, None] * E + lane).reshape(-1)
+    out = (normal_f64(stream_key(seed, tag, "small", agent, layer), ctr) * 1.0e-3).reshape(len(tokens), E)
+    if pr.any():
+        ctr_big = (tokens[pr][:, None] * E + lane).reshape(-1)
+        out[pr] += (normal_f64(stream_key(seed, tag, "big", agent, layer), ctr_big) * 0.5).reshape(-1, E)
+    return out.astype(np.float32)
+
+
+def check_noise(rnd: Round, seed: Optional[int] = None) -> np.ndarray:
+    """[N][S][E] float32: added to each agent's reused K at the check layer to make the
+    'fresh' K the selection compares against."""
+    cfg = rnd.cfg
+    seed = cfg.seed if seed is None else seed
+    N, S, E = cfg.n_agents, cfg.n_shared, cfg.elems
+    out = np.empty((N, S, E), dtype=np.float32)
+    for i in range(N):
+        out[i] = _noise_rows(seed, "chk", i, cfg.check_layer, np.arange(S), rnd.perturbed[i], E)
+    return out
+
+
+def selected_noise(rnd: Round, sel: np.ndarray, layers=None, seed: Optional[int] = None):
+    """Noise for the fresh K and V at the selected tokens of every layer:
+    two float32 arrays [N][len(layers)][k][E], keyed by (agent, layer, token), so the
+    values do not depend on how the selection is stored."""
+    cfg = rnd.cfg
+    seed = cfg.seed if seed is None else seed
+    layers = range(cfg.n_layers) if layers is None else layers
+    N, E = cfg.n_agents, cfg.elems
+    k = sel.shape[1]
+    nk = np.empty((N, len(layers), k, E), dtype=np.float32)
+    nv = np.empty_like(nk)
+    for i in range(N):
+        pr = rnd.perturbed[i, sel[i]] if k else np.zeros(0, bool)
+        for li, l in enumerate(layers):
+            nk[i, li] = _noise_rows(seed, "selK", i, l, sel[i], pr, E)
+            nv[i, li] = _noise_rows(seed, "selV", i, l, sel[i], pr, E)
+    return nk, nv
+
+
+def add_noise_bf16(base_bits: np.ndarray, noise: np.ndarray) -> np.ndarray:
+    """bf16(float32(base) + noise), round to nearest even: a synthetic 'recomputed' value."""
+    return f32_to_bf16_bits(bf16_bits_to_f32(base_bits) + noise)

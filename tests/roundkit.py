@@ -1,0 +1,120 @@
+"""Test-side assembly of a synthetic round and of the oracle's full chain.
+
+The synthetic 'recomputed' K/V are the reused values plus the generator's noise, which is
+how the workloads describe them (fresh K = reused K + small noise, large noise on the
+perturbed tokens). Everything here runs on the CPU through the oracle.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+import oracle as _oracle
+from collective_kv_cache_gb300 import synth
+
+
+def token_layout(block_len):
+    """canonical start of each block, and block / local index of each canonical token"""
+    bl = np.asarray(block_len, dtype=np.int64)
+    start = np.concatenate([[0], np.cumsum(bl)[:-1]])
+    tok_block = np.repeat(np.arange(len(bl)), bl)
+    u = np.arange(int(bl.sum())) - start[tok_block]
+    return start, tok_block, u
+
+
+def positions(off: np.ndarray, block_len) -> np.ndarray:
+    """[N][S]: prompt position of canonical token t in agent i."""
+    _, tb, u = token_layout(block_len)
+    return off[:, tb] + u[None, :]
+
+
+def gather_rows(pool: np.ndarray, block_table: np.ndarray, P: int, agent: int, layer: int,
+                kv: int, pos: np.ndarray) -> np.ndarray:
+    """Rows of one agent's paged cache at prompt positions pos -> [len(pos)][E]."""
+    pages = block_table[agent, pos // P]
+    assert (pages >= 0).all()
+    rows = pool[layer, kv, pages, pos % P]          # [n][H][D]
+    return rows.reshape(len(pos), pool.shape[4] * pool.shape[5])
+
+
+@dataclasses.dataclass
+class Chain:
+    cfg: synth.RoundConfig
+    rnd: synth.Round
+    desc: tuple                 # (block_len, hist_len, perm)
+    off: np.ndarray
+    pos: np.ndarray             # [N][S]
+    kc: np.ndarray
+    vc: np.ndarray
+    pool_after_rerotate: Optional[np.ndarray] = None
+    k_fresh: Optional[np.ndarray] = None      # [N][S][E]
+    sel: Optional[np.ndarray] = None
+    dev: Optional[np.ndarray] = None
+    master: Optional[int] = None
+    cost: Optional[np.ndarray] = None
+    k_fresh_sel: Optional[np.ndarray] = None  # [N][L][k][E]
+    v_fresh_sel: Optional[np.ndarray] = None
+    store: Optional[dict] = None
+    pool_after_restore: Optional[np.ndarray] = None
+
+
+def make_inputs(cfg: synth.RoundConfig, seed: Optional[int] = None, orc=None) -> Chain:
+    orc = orc or _oracle.get()
+    rnd = synth.make_round(cfg, seed)
+    desc = (rnd.block_len, rnd.hist_len, rnd.perm)
+    off = orc.offsets(*desc)
+    kc, vc = synth.canonical_kv(cfg, seed)
+    return Chain(cfg, rnd, desc, off, positions(off, rnd.block_len), kc, vc)
+
+
+def fresh_check(ch: Chain, pool: np.ndarray) -> np.ndarray:
+    """Synthetic recomputed K at the check layer: reused K + check-layer noise."""
+    cfg, rnd = ch.cfg, ch.rnd
+    noise = synth.check_noise(rnd)
+    out = np.empty((cfg.n_agents, cfg.n_shared, cfg.elems), dtype=np.uint16)
+    for i in range(cfg.n_agents):
+        reused = gather_rows(pool, rnd.block_table, cfg.page_size, i, cfg.check_layer, 0, ch.pos[i])
+        out[i] = synth.add_noise_bf16(reused, noise[i])
+    return out
+
+
+def fresh_selected(ch: Chain, pool: np.ndarray, sel: np.ndarray):
+    """Synthetic recomputed K (agent frame) and V at the selected tokens of every layer."""
+    cfg, rnd = ch.cfg, ch.rnd
+    nk, nv = synth.selected_noise(rnd, sel)
+    N, L, k, E = cfg.n_agents, cfg.n_layers, sel.shape[1], cfg.elems
+    kf = np.empty((N, L, k, E), dtype=np.uint16)
+    vf = np.empty((N, L, k, E), dtype=np.uint16)
+    for i in range(N):
+        for l in range(L):
+            reused = gather_rows(pool, rnd.block_table, cfg.page_size, i, l, 0, ch.pos[i, sel[i]])
+            kf[i, l] = synth.add_noise_bf16(reused, nk[i, l])
+            vf[i, l] = synth.add_noise_bf16(ch.vc[l, sel[i]], nv[i, l])
+    return kf, vf
+
+
+def run_oracle_chain(ch: Chain, restore: bool = True, orc=None, frame: int = 0) -> Chain:
+    orc = orc or _oracle.get()
+    cfg, rnd = ch.cfg, ch.rnd
+    pool = _oracle.new_pool(cfg, rnd.num_pages)
+    st = orc.rerotate(cfg, ch.desc, ch.kc, ch.vc, pool, rnd.num_pages, rnd.block_table)
+    assert st == 0, st
+    ch.pool_after_rerotate = pool.copy()
+    ch.k_fresh = fresh_check(ch, pool)
+    st, ch.sel, ch.dev = orc.check_select(cfg, ch.desc, pool, rnd.num_pages, rnd.block_table,
+                                          ch.k_fresh)
+    assert st == 0, st
+    ch.master, ch.cost = orc.pick_master(cfg.n_shared, cfg.diff_block, ch.sel)
+    ch.k_fresh_sel, ch.v_fresh_sel = fresh_selected(ch, pool, ch.sel)
+    ch.store = orc.diff_encode(cfg, ch.desc, ch.master, ch.kc, ch.vc, ch.sel, ch.k_fresh_sel,
+                               ch.v_fresh_sel)
+    assert ch.store["status"] == 0, ch.store["status"]
+    if restore:
+        pool2 = _oracle.new_pool(cfg, rnd.num_pages)
+        st = orc.fused_restore(cfg, ch.desc, ch.master, ch.store, np.arange(cfg.n_agents),
+                               pool2, rnd.num_pages, rnd.block_table, frame=frame)
+        assert st == 0, st
+        ch.pool_after_restore = pool2
+    return ch
