@@ -1,0 +1,483 @@
+#!/usr/bin/env python3
+"""Benchmark of the collective KV path on GB300: one step = one All-Gather round through
+all four stages (re-rotation of the shared blocks into every agent's paged KV, check-layer
+deviation and selection, master choice and Master-Mirror encoding, fused restore of every
+agent's paged KV), on the Qwen2.5-7B-shaped round: 10 agents, 28 layers, 4 KV heads x 128,
+10 shared blocks of 256 tokens, histories uniform on 500..4000 tokens.
+
+Prints one JSON line (rank 0). `value` is the algorithmic HBM bytes of the whole step
+divided by its device time, in GB/s; agent-rounds/s and the fraction of the measured HBM
+peak ride along. The recompute of the selected tokens (a model forward) is outside the
+path: its synthetic stand-in is prepared before timing and stays resident.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Under torchrun every rank runs its own independent round (weak scaling, no collective on
+the data path); the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "restore+reuse KV GB/s (% of GB300 HBM peak); agent-rounds/sec, 7B shape"
+UNIT = "GB/s"
+LAUNCHES_PER_STEP = 11   # rerotate 1, deviation+select 2, master 1, encode 6, restore 1
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+# ------------------------------------------------------------------ shared host logic
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank processes its own independent round."""
+    return base_seed + 7919 * rank
+
+
+def reduce_max(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def stage_bytes(cfg, n_agents: int, nl: int, k: int, nnz: int, n_restored: int) -> dict:
+    """Algorithmic HBM bytes of each stage: what the method must move, counted once."""
+    S, E, B = cfg.n_shared, cfg.elems, cfg.diff_block
+    row = S * E * 2                       # one layer of one tensor, bf16
+    rec = B * E * 4 + 4                   # one diff record: K and V values and its index
+    return {
+        "rerotate": 2 * nl * row + n_agents * 2 * nl * row,
+        "select": 2 * n_agents * S * E * 2,
+        "master": n_agents * k * 4,
+        "encode": n_agents * nl * k * E * 4 + 2 * nl * row + 2 * nl * row + nnz * rec,
+        "restore": 2 * nl * row + nnz * rec + n_restored * 2 * nl * row,
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    def __init__(self, gpu_index: str):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        if not self.proc:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], f[5:9]):
+                if val.lower() in ("active", "0x1", "1"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def setup_round(cfg, seed, device):
+    import torch
+    from collective_kv_cache_gb300 import runner as R
+    from collective_kv_cache_gb300 import synth
+
+    rnd = synth.make_round(cfg, seed)
+    kc_bits, vc_bits = synth.canonical_kv(cfg, seed)
+    rr = R.RoundRunner(cfg, rnd.block_len, rnd.hist_len, rnd.perm, rnd.block_table,
+                       rnd.num_pages, device=device)
+    kc = R.to_device_bf16(kc_bits, device)
+    vc = R.to_device_bf16(vc_bits, device)
+    del kc_bits, vc_bits
+    # Synthetic stand-in for the model's recompute (outside the path): reused K plus noise.
+    rr.rerotate(kc, vc)
+    pos = rr.positions()
+    N, L, E, P = cfg.n_agents, cfg.n_layers, cfg.elems, cfg.page_size
+    noise = synth.check_noise(rnd, seed)
+    kf = torch.empty((N, cfg.n_shared, E), dtype=torch.bfloat16, device=device)
+    for i in range(N):
+        kf[i] = (rr.gather(i, cfg.check_layer, 0, pos[i]).float()
+                 + torch.from_numpy(noise[i]).to(device)).to(torch.bfloat16)
+    del noise
+    sel = rr.check_select(kf)
+    master = rr.pick_master()
+    sel_np = sel.cpu().numpy()
+    k = sel_np.shape[1]
+    nk, nv = synth.selected_noise(rnd, sel_np, seed=seed)
+    kfs = torch.empty((N, L, k, E), dtype=torch.bfloat16, device=device)
+    vfs = torch.empty((N, L, k, E), dtype=torch.bfloat16, device=device)
+    for i in range(N):
+        p = torch.from_numpy(pos[i, sel_np[i]].astype(np.int64)).to(device)
+        pages = rr.bt_t[i].long()[p // P]
+        reused = rr.pool_t[:, 0, pages, p % P].reshape(L, k, E)
+        kfs[i] = (reused.float() + torch.from_numpy(nk[i]).to(device)).to(torch.bfloat16)
+        t = torch.from_numpy(sel_np[i].astype(np.int64)).to(device)
+        vfs[i] = (vc[:, t].float() + torch.from_numpy(nv[i]).to(device)).to(torch.bfloat16)
+    del nk, nv
+    bound = rr.candidate_bound(master)
+    rr.alloc_store(max(bound, 1))
+    nnz = rr.diff_encode(kc, vc, kfs, vfs)
+    torch.cuda.synchronize()
+    return dict(rr=rr, kc=kc, vc=vc, kf=kf, kfs=kfs, vfs=vfs, k=k, nnz=nnz, master=master,
+                rnd=rnd)
+
+
+def run_step(st, agents, events=None):
+    rr = st["rr"]
+    s = rr.stream
+    if events is not None:
+        events[0].record(s)
+    rr.rerotate(st["kc"], st["vc"])
+    if events is not None:
+        events[1].record(s)
+    rr.check_select(st["kf"])
+    if events is not None:
+        events[2].record(s)
+    rr.pick_master(want_host=False)
+    if events is not None:
+        events[3].record(s)
+    rr.diff_encode(st["kc"], st["vc"], st["kfs"], st["vfs"], want_nnz=False)
+    if events is not None:
+        events[4].record(s)
+    rr.fused_restore(agents, frame=0)
+    if events is not None:
+        events[5].record(s)
+
+
+STAGES = ("rerotate", "select", "master", "encode", "restore")
+
+
+def bench_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from collective_kv_cache_gb300 import build as _build
+    from collective_kv_cache_gb300 import synth
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    cfg = synth.CONFIGS[args.workload]()
+    seed = rank_seed(cfg.seed, rank)
+    st = setup_round(cfg, seed, device)
+    rr = st["rr"]
+    agents = list(range(cfg.n_agents))
+    N, L = cfg.n_agents, cfg.n_layers
+
+    for _ in range(args.warmup):
+        run_step(st, agents)
+    torch.cuda.synchronize()
+    s, bits = rr.get_error()
+    if s != 0:
+        raise RuntimeError(f"device error word {bits:#x} after warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] \
+        if world == 1 else str(local_rank)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id if gpu_id.isdigit() else "0") as clk:
+        start.record(rr.stream)
+        for i in range(K):
+            run_step(st, agents, evs[i])
+        end.record(rr.stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = start.elapsed_time(end)
+    ms_max = reduce_max(ms_total, device)
+    stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
+                for j, name in enumerate(STAGES)}
+    s, bits = rr.get_error()
+    if s != 0:
+        raise RuntimeError(f"device error word {bits:#x} in the timed region")
+
+    by = stage_bytes(cfg, N, L, st["k"], st["nnz"], N)
+    step_bytes = sum(by.values())
+    total_bytes = reduce_sum(float(step_bytes) * K, device)
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    ms_per_step = ms_max / K
+    agent_rounds = reduce_sum(float(N) * K, device) / (ms_max * 1e-3)
+
+    # dominant single-kernel stage for the roofline
+    dom = max(("rerotate", "restore"), key=lambda n: stage_ms[n])
+    achieved = by[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                tj = json.load(f)
+            traffic = tj.get(args.workload, {}).get(dom)
+        except Exception:
+            traffic = None
+
+    e2e = bench_e2e(st, agents, cfg, K, device) if not args.no_e2e else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, seed, layers=args.cpu_layers)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "agents": N, "layers": L,
+                       "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
+                       "shared_tokens": cfg.n_shared, "shared_blocks": cfg.n_blocks,
+                       "page_size": cfg.page_size, "recompute_pct": cfg.recompute_pct,
+                       "history": list(cfg.hist_range), "parallelism": f"independent rounds x{world}",
+                       "l2": "inputs larger than L2 (step moves %.2f GB); no flush" % (step_bytes / 1e9)},
+            "agent_rounds_per_s": round(agent_rounds, 1),
+            "hbm_frac_of_peak": round(value / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
+            "stages": {n: {"ms": round(stage_ms[n], 5), "bytes": by[n],
+                           "gbs": round(by[n] / (stage_ms[n] * 1e-3) / 1e9, 1)} for n in STAGES},
+            "diff_blocks": st["nnz"], "selected_per_agent": st["k"], "master": st["master"],
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "peak_kind": peak_kind},
+            "e2e": e2e,
+            "gpu_launches": LAUNCHES_PER_STEP * K,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def bench_e2e(st, agents, cfg, K, device):
+    """Same step through the public calls with HOST inputs: pinned host -> device copies of
+    the round's inputs and a device -> host read of its result inside the timed region."""
+    import torch
+
+    rr = st["rr"]
+    names = ("kc", "vc", "kf", "kfs", "vfs")
+    host = {n: torch.empty(st[n].shape, dtype=st[n].dtype, pin_memory=True) for n in names}
+    for n in names:
+        host[n].copy_(st[n])
+    res = {"rowptr": rr.store_t["rowptr"], "sel": rr.sel_t, "master": rr.master_t}
+    res_h = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in res.items()}
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = sum(t.numel() * t.element_size() for t in res.values())
+    s = rr.stream
+
+    def one():
+        with torch.cuda.stream(s):
+            for n in names:
+                st[n].copy_(host[n], non_blocking=True)
+        run_step(st, agents)
+        with torch.cuda.stream(s):
+            for n, t in res.items():
+                res_h[n].copy_(t, non_blocking=True)
+        s.synchronize()
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(K):
+        one()
+    b.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    by = sum(stage_bytes(cfg, cfg.n_agents, cfg.n_layers, st["k"], st["nnz"],
+                         cfg.n_agents).values())
+    return {"value": round(by * K / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "ms_per_step": round(ms / K, 4), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------ the oracle on host cores
+def oracle_round(cfg, seed, layers):
+    """Inputs for the oracle restricted to the first `layers` layers (check layer inside)."""
+    import oracle
+    from collective_kv_cache_gb300 import synth
+    sub = cfg.replace(n_layers=layers)
+    rnd = synth.make_round(sub, seed)
+    kc, vc = synth.canonical_kv(sub, seed)
+    return sub, rnd, kc, vc, oracle.get()
+
+
+def oracle_step(sub, rnd, kc, vc, orc, cache):
+    """One oracle pass over the sample; returns (seconds inside oracle calls, k, nnz).
+    The synthetic recompute (reused K plus noise) is built on the first pass and reused;
+    it is not timed."""
+    import oracle
+    from tests import roundkit as rk  # test-side assembly of the synthetic recompute
+    desc = (rnd.block_len, rnd.hist_len, rnd.perm)
+    if "chain" not in cache:
+        off = orc.offsets(*desc)
+        cache["chain"] = rk.Chain(sub, rnd, desc, off, rk.positions(off, rnd.block_len), kc, vc)
+    ch = cache["chain"]
+    pool = oracle.new_pool(sub, rnd.num_pages)
+    t0 = time.perf_counter()
+    assert orc.rerotate(sub, desc, kc, vc, pool, rnd.num_pages, rnd.block_table) == 0
+    secs = time.perf_counter() - t0
+    if "kf" not in cache:
+        cache["kf"] = rk.fresh_check(ch, pool)
+    t0 = time.perf_counter()
+    st, sel, _ = orc.check_select(sub, desc, pool, rnd.num_pages, rnd.block_table, cache["kf"])
+    m, _ = orc.pick_master(sub.n_shared, sub.diff_block, sel)
+    secs += time.perf_counter() - t0
+    if "kfs" not in cache:
+        cache["kfs"], cache["vfs"] = rk.fresh_selected(ch, pool, sel)
+    pool2 = oracle.new_pool(sub, rnd.num_pages)
+    t0 = time.perf_counter()
+    store = orc.diff_encode(sub, desc, m, kc, vc, sel, cache["kfs"], cache["vfs"])
+    orc.fused_restore(sub, desc, m, store, np.arange(sub.n_agents), pool2, rnd.num_pages,
+                      rnd.block_table)
+    secs += time.perf_counter() - t0
+    return secs, sel.shape[1], store["nnz"]
+
+
+def cpu_baseline(cfg, seed, layers):
+    sub, rnd, kc, vc, orc = oracle_round(cfg, seed, layers)
+    cache = {}
+    secs, k, nnz = oracle_step(sub, rnd, kc, vc, orc, cache)
+    by = sum(stage_bytes(sub, sub.n_agents, layers, k, nnz, sub.n_agents).values())
+    return {"value": round(by / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "seconds": round(secs, 2),
+            "sample": f"the same round restricted to layers 0..{layers - 1} of {cfg.n_layers} "
+                      f"(all {cfg.n_agents} agents, all {cfg.n_shared} shared tokens), one "
+                      f"single-threaded pass of the plain C oracle"}
+
+
+def bench_reference(args, rank, world):
+    """The reference arm: the oracle as it stands, on the host cores, same metric."""
+    if rank != 0:
+        return
+    from collective_kv_cache_gb300 import synth
+    cfg = synth.CONFIGS[args.workload]()
+    layers = args.ref_layers
+    sub, rnd, kc, vc, orc = oracle_round(cfg, cfg.seed, layers)
+    cache = {}
+    for _ in range(args.warmup):
+        oracle_step(sub, rnd, kc, vc, orc, cache)
+    tot, k, nnz = 0.0, 0, 0
+    for _ in range(args.steps):
+        secs, k, nnz = oracle_step(sub, rnd, kc, vc, orc, cache)
+        tot += secs
+    by = sum(stage_bytes(sub, sub.n_agents, layers, k, nnz, sub.n_agents).values())
+    value = by * args.steps / tot / 1e9
+    sample = (f"each step: the round restricted to layers 0..{layers - 1} of {cfg.n_layers}, "
+              f"all agents and tokens, single-threaded plain C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "agents": cfg.n_agents, "layers": cfg.n_layers,
+                   "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
+                   "shared_tokens": cfg.n_shared, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="qwen7b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-layers", type=int, default=12)
+    ap.add_argument("--ref-layers", type=int, default=4)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        bench_reference(args, rank, world)
+    else:
+        bench_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

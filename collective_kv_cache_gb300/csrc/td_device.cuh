@@ -1,0 +1,117 @@
+// td_device.cuh - device helpers: bf16 packing, the RoPE pair-vector rotation, tile
+// geometry and the paged-KV address of a token row.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "td_internal.h"
+
+namespace td {
+
+// ---- bf16 words: a 32-bit word holds two bf16 values, the lower address in the low half.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two floats -> two bf16, round to nearest even, in one instruction.
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* x) {
+  x[0] = bf_lo(v.x); x[1] = bf_hi(v.x); x[2] = bf_lo(v.y); x[3] = bf_hi(v.y);
+  x[4] = bf_lo(v.z); x[5] = bf_hi(v.z); x[6] = bf_lo(v.w); x[7] = bf_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* y) {
+  return make_uint4(pack_bf2(y[0], y[1]), pack_bf2(y[2], y[3]), pack_bf2(y[4], y[5]),
+                    pack_bf2(y[6], y[7]));
+}
+
+__device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ uint4 ld16(const uint16_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ void st16(uint16_t* p, const uint4& v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+__device__ __forceinline__ bool neq16(const uint4& a, const uint4& b) {
+  return ((a.x ^ b.x) | (a.y ^ b.y) | (a.z ^ b.z) | (a.w ^ b.w)) != 0u;
+}
+
+// ---- RoPE on one pair-vector: 8 consecutive frequencies f0..f0+7 of one head.
+// a holds elements f0..f0+7, b holds f0+D/2..f0+D/2+7; c, s point at cos/sin[f0].
+// forward:  y0 = fma(x0, c, -(x1*s)),  y1 = fma(x1, c, x0*s)
+// inverse:  y0 = fma(x0, c,  x1*s),    y1 = fma(x1, c, -(x0*s))
+// Each cross product is rounded to float before the fma; outputs rounded to bf16.
+template <bool kInverse>
+__device__ __forceinline__ void rotate_pairs(const uint4& a, const uint4& b, const float* c,
+                                             const float* s, uint4& ya, uint4& yb) {
+  float x0[8], x1[8], y0[8], y1[8];
+  unpack8(a, x0);
+  unpack8(b, x1);
+  const float4 c0 = __ldg(reinterpret_cast<const float4*>(c));
+  const float4 c1 = __ldg(reinterpret_cast<const float4*>(c) + 1);
+  const float4 s0 = __ldg(reinterpret_cast<const float4*>(s));
+  const float4 s1 = __ldg(reinterpret_cast<const float4*>(s) + 1);
+  const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float x1s = __fmul_rn(x1[q], ss[q]);
+    const float x0s = __fmul_rn(x0[q], ss[q]);
+    if (kInverse) {
+      y0[q] = __fmaf_rn(x0[q], cc[q], x1s);
+      y1[q] = __fmaf_rn(x1[q], cc[q], -x0s);
+    } else {
+      y0[q] = __fmaf_rn(x0[q], cc[q], -x1s);
+      y1[q] = __fmaf_rn(x1[q], cc[q], x0s);
+    }
+  }
+  ya = pack8(y0);
+  yb = pack8(y1);
+}
+
+// ---- Tile geometry: a tile is (layer, 16 canonical tokens); item q of a tile is the
+// pair-vector g = q % vpt of token q / vpt. Element offsets within the token row:
+//   e0 = h*D + fg*8 (first half of head h), e1 = e0 + D/2, with h = g / (D/16),
+//   fg = g % (D/16); the table offset of the item is fg*8.
+struct Item {
+  int tok;   // 0..15 within the tile
+  int e0;    // element offset of the first-half vector
+  int f0;    // first frequency
+};
+
+__device__ __forceinline__ Item item_of(const Geom& g, int q) {
+  Item it;
+  it.tok = q / g.vpt;
+  const int gv = q - it.tok * g.vpt;
+  const int per_head = g.D >> 4;
+  const int h = gv / per_head;
+  it.f0 = (gv - h * per_head) * 8;
+  it.e0 = h * g.D + it.f0;
+  return it;
+}
+
+// Row address of (agent, layer, kv, position) in the paged pool, or nullptr (and the
+// error bit) when the page is unmapped or out of range.
+__device__ __forceinline__ uint16_t* pool_row(const PoolDev& p, int E, int agent, int layer,
+                                              int kv, int pos, uint32_t* err) {
+  const int lp = p.p_shift >= 0 ? (pos >> p.p_shift) : pos / p.P;
+  const int slot = pos - lp * p.P;
+  int32_t page = -1;
+  if (lp < p.max_lp) page = __ldg(p.bt + static_cast<int64_t>(agent) * p.max_lp + lp);
+  if (page < 0 || page >= p.num_pages) {
+    atomicOr(err, err_bit(TD_ERR_UNMAPPED_PAGE));
+    return nullptr;
+  }
+  const int64_t row = ((static_cast<int64_t>(layer) * 2 + kv) * p.num_pages + page) * p.P + slot;
+  return p.base + row * E;
+}
+
+}  // namespace td

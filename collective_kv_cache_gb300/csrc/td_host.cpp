@@ -1,0 +1,521 @@
+// td_host.cpp - the C ABI (include/td.h): argument validation, the context and its
+// scratch, the round's offset and RoPE tables, and the kernel launches.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "td.h"
+#include "td_internal.h"
+
+using namespace td;
+
+struct td_ctx {
+  td_shape shape;
+  Geom g;
+  int max_agents, max_blocks, max_shared, max_nb, nbw_max;
+  int device;
+
+  // round tables (device) and their pinned staging
+  int32_t* d_off = nullptr;
+  float* d_cos = nullptr;
+  float* d_sin = nullptr;
+  int32_t* d_tok_block = nullptr;
+  int32_t* d_blk_start = nullptr;
+  unsigned char* h_stage = nullptr;
+  size_t stage_bytes = 0;
+  cudaEvent_t stage_done = nullptr;
+  bool stage_pending = false;
+
+  // cached round (host copy) and its device view
+  bool have_round = false;
+  int N = 0, M = 0, S = 0;
+  std::vector<int32_t> c_len, c_hist, c_perm;
+
+  // scratch
+  float* d_dev = nullptr;           // [max_agents * max_shared]
+  int32_t* d_rank = nullptr;        // [max_agents * max_shared]
+  uint32_t* d_mask = nullptr;       // [max_agents * nbw_max]
+  uint32_t* d_cand = nullptr;       // [max_agents * nbw_max]
+  int32_t* d_wprefix = nullptr;     // [max_agents * nbw_max + max_agents]
+  int64_t* d_aprefix = nullptr;     // [max_agents + 1]
+  uint8_t* d_flag = nullptr;        // [max_agents * L * max_nb]
+  int32_t* d_ints = nullptr;        // need_fixup, m_ok, over, spare
+  int64_t* d_bound = nullptr;
+  uint32_t* d_err = nullptr;
+  // pinned host words for results
+  int64_t* h_words = nullptr;       // [4]
+};
+
+namespace {
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int log2i(int x) {
+  int s = 0;
+  while ((1 << s) < x) ++s;
+  return s;
+}
+
+td_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TD_OK : TD_ERR_CUDA; }
+
+void free_ctx(td_ctx* c) {
+  if (!c) return;
+  cudaFree(c->d_off);
+  cudaFree(c->d_cos);
+  cudaFree(c->d_sin);
+  cudaFree(c->d_tok_block);
+  cudaFree(c->d_blk_start);
+  cudaFree(c->d_dev);
+  cudaFree(c->d_rank);
+  cudaFree(c->d_mask);
+  cudaFree(c->d_cand);
+  cudaFree(c->d_wprefix);
+  cudaFree(c->d_aprefix);
+  cudaFree(c->d_flag);
+  cudaFree(c->d_ints);
+  cudaFree(c->d_bound);
+  cudaFree(c->d_err);
+  if (c->h_stage) cudaFreeHost(c->h_stage);
+  if (c->h_words) cudaFreeHost(c->h_words);
+  if (c->stage_done) cudaEventDestroy(c->stage_done);
+  delete c;
+}
+
+bool same_device(const td_ctx* c) {
+  int d = -1;
+  return cudaGetDevice(&d) == cudaSuccess && d == c->device;
+}
+
+// Validates the round and brings the device tables up to date with it.
+td_status prepare_round(td_ctx* c, const td_round* r, cudaStream_t st) {
+  if (!r || !r->block_len || !r->hist_len || !r->perm) return TD_ERR_INVALID_ARG;
+  const int N = r->n_agents, M = r->n_blocks;
+  if (N < 1 || N > c->max_agents || M < 1 || M > c->max_blocks) return TD_ERR_INVALID_ARG;
+  int64_t S = 0;
+  for (int j = 0; j < M; ++j) {
+    if (r->block_len[j] < 1) return TD_ERR_INVALID_ARG;
+    S += r->block_len[j];
+  }
+  if (S > c->max_shared) return TD_ERR_INVALID_ARG;
+  for (int i = 0; i < N; ++i) {
+    if (r->hist_len[i] < 0 || static_cast<int64_t>(r->hist_len[i]) + S > INT32_MAX / 2)
+      return TD_ERR_INVALID_ARG;
+    std::vector<char> seen(M, 0);
+    for (int q = 0; q < M; ++q) {
+      const int j = r->perm[static_cast<int64_t>(i) * M + q];
+      if (j < 0 || j >= M || seen[j]) return TD_ERR_INVALID_ARG;
+      seen[j] = 1;
+    }
+  }
+  if (c->have_round && c->N == N && c->M == M &&
+      std::memcmp(c->c_len.data(), r->block_len, sizeof(int32_t) * M) == 0 &&
+      std::memcmp(c->c_hist.data(), r->hist_len, sizeof(int32_t) * N) == 0 &&
+      std::memcmp(c->c_perm.data(), r->perm, sizeof(int32_t) * N * M) == 0)
+    return TD_OK;
+
+  // the previous upload must have left the staging buffer before it is rewritten
+  if (c->stage_pending) {
+    if (cudaEventSynchronize(c->stage_done) != cudaSuccess) return TD_ERR_CUDA;
+    c->stage_pending = false;
+  }
+  const int half = c->g.half;
+  const size_t n_off = static_cast<size_t>(N) * M;
+  unsigned char* p = c->h_stage;
+  int32_t* off = reinterpret_cast<int32_t*>(p);
+  float* cs = reinterpret_cast<float*>(off + n_off);
+  float* sn = cs + n_off * half;
+  int32_t* tokb = reinterpret_cast<int32_t*>(sn + n_off * half);
+  int32_t* bst = tokb + S;
+  // offsets: history, then the blocks in the agent's order
+  for (int i = 0; i < N; ++i) {
+    int64_t pos = r->hist_len[i];
+    for (int q = 0; q < M; ++q) {
+      const int j = r->perm[static_cast<int64_t>(i) * M + q];
+      off[static_cast<int64_t>(i) * M + j] = static_cast<int32_t>(pos);
+      pos += r->block_len[j];
+    }
+  }
+  // RoPE tables: angle = off * theta^(-2f/D) in float64, cos/sin rounded once to float
+  std::vector<double> inv_freq(half);
+  for (int f = 0; f < half; ++f)
+    inv_freq[f] = std::pow(c->shape.rope_theta,
+                           -static_cast<double>(2 * f) / static_cast<double>(c->g.D));
+  for (size_t ab = 0; ab < n_off; ++ab) {
+    const double a = static_cast<double>(off[ab]);
+    for (int f = 0; f < half; ++f) {
+      const double ang = a * inv_freq[f];
+      cs[ab * half + f] = static_cast<float>(std::cos(ang));
+      sn[ab * half + f] = static_cast<float>(std::sin(ang));
+    }
+  }
+  int64_t s0 = 0;
+  for (int j = 0; j < M; ++j) {
+    bst[j] = static_cast<int32_t>(s0);
+    for (int u = 0; u < r->block_len[j]; ++u) tokb[s0 + u] = j;
+    s0 += r->block_len[j];
+  }
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(c->d_off, off, n_off * 4, cudaMemcpyHostToDevice, st)) ||
+      (e = cudaMemcpyAsync(c->d_cos, cs, n_off * half * 4, cudaMemcpyHostToDevice, st)) ||
+      (e = cudaMemcpyAsync(c->d_sin, sn, n_off * half * 4, cudaMemcpyHostToDevice, st)) ||
+      (e = cudaMemcpyAsync(c->d_tok_block, tokb, S * 4, cudaMemcpyHostToDevice, st)) ||
+      (e = cudaMemcpyAsync(c->d_blk_start, bst, M * 4, cudaMemcpyHostToDevice, st)) ||
+      (e = cudaEventRecord(c->stage_done, st)))
+    return TD_ERR_CUDA;
+  c->stage_pending = true;
+  c->have_round = true;
+  c->N = N;
+  c->M = M;
+  c->S = static_cast<int>(S);
+  c->c_len.assign(r->block_len, r->block_len + M);
+  c->c_hist.assign(r->hist_len, r->hist_len + N);
+  c->c_perm.assign(r->perm, r->perm + static_cast<size_t>(N) * M);
+  return TD_OK;
+}
+
+RoundDev round_dev(const td_ctx* c) {
+  RoundDev rd;
+  rd.N = c->N;
+  rd.M = c->M;
+  rd.S = c->S;
+  rd.nb = (c->S + kDiffBlock - 1) / kDiffBlock;
+  rd.off = c->d_off;
+  rd.cos_t = c->d_cos;
+  rd.sin_t = c->d_sin;
+  rd.tok_block = c->d_tok_block;
+  rd.blk_start = c->d_blk_start;
+  return rd;
+}
+
+// The pool must map every shared position: hist + S - 1 fits the block table.
+td_status pool_dev(const td_ctx* c, const td_round* r, const td_paged* p, PoolDev* out) {
+  if (!p || !p->base || !p->block_table || p->num_pages < 1 || p->max_pages_per_agent < 1)
+    return TD_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(p->base) & 15u) != 0) return TD_ERR_INVALID_ARG;
+  const int P = c->shape.page_size;
+  for (int i = 0; i < r->n_agents; ++i) {
+    const int64_t last = static_cast<int64_t>(r->hist_len[i]) + c->S - 1;
+    if (last / P >= p->max_pages_per_agent) return TD_ERR_INVALID_ARG;
+  }
+  out->base = static_cast<uint16_t*>(p->base);
+  out->num_pages = p->num_pages;
+  out->bt = p->block_table;
+  out->max_lp = p->max_pages_per_agent;
+  out->P = P;
+  out->p_shift = is_pow2(P) ? log2i(P) : -1;
+  return TD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* td_status_string(td_status s) {
+  switch (s) {
+    case TD_OK: return "ok";
+    case TD_ERR_INVALID_ARG: return "invalid argument";
+    case TD_ERR_CUDA: return "CUDA error";
+    case TD_ERR_CAPACITY: return "diff store capacity exceeded";
+    case TD_ERR_UNMAPPED_PAGE: return "unmapped or out-of-range page";
+    case TD_ERR_NONFINITE: return "non-finite key deviation";
+    case TD_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_blocks,
+                        int32_t max_shared, td_ctx** out) {
+  if (!shape || !out) return TD_ERR_INVALID_ARG;
+  *out = nullptr;
+  const td_shape& s = *shape;
+  if (s.n_layers < 1 || s.n_kv_heads < 1 || s.head_dim < 16 || s.head_dim % 16 != 0 ||
+      s.page_size < 1 || s.diff_block != kDiffBlock || !(s.rope_theta > 1.0) ||
+      !std::isfinite(s.rope_theta))
+    return TD_ERR_INVALID_ARG;
+  const int64_t E = static_cast<int64_t>(s.n_kv_heads) * s.head_dim;
+  if (E > 2048) return TD_ERR_INVALID_ARG;  // a tile holds 16 rows of at most 2048 elements
+  if (max_agents < 1 || max_blocks < 1 || max_shared < 1 || max_agents > 4096 ||
+      max_shared > (1 << 22))
+    return TD_ERR_INVALID_ARG;
+  const int max_nb = (max_shared + kDiffBlock - 1) / kDiffBlock;
+  const int nbw = (max_nb + 31) / 32;
+  // one-CTA kernels keep per-agent masks and per-row counts in shared memory
+  if (static_cast<int64_t>(max_agents) * nbw * 4 + 8 * max_agents > 160 * 1024) return TD_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_agents) * s.n_layers * 8 > 160 * 1024) return TD_ERR_INVALID_ARG;
+
+  td_ctx* c = new (std::nothrow) td_ctx;
+  if (!c) return TD_ERR_CUDA;
+  c->shape = s;
+  c->g.H = s.n_kv_heads;
+  c->g.D = s.head_dim;
+  c->g.E = static_cast<int>(E);
+  c->g.half = s.head_dim / 2;
+  c->g.vpt = static_cast<int>(E / 16);
+  c->max_agents = max_agents;
+  c->max_blocks = max_blocks;
+  c->max_shared = max_shared;
+  c->max_nb = max_nb;
+  c->nbw_max = nbw;
+  if (cudaGetDevice(&c->device) != cudaSuccess) {
+    delete c;
+    return TD_ERR_CUDA;
+  }
+  const size_t NM = static_cast<size_t>(max_agents) * max_blocks;
+  const size_t half = c->g.half;
+  const size_t NS = static_cast<size_t>(max_agents) * max_shared;
+  c->stage_bytes = NM * 4 + 2 * NM * half * 4 + static_cast<size_t>(max_shared) * 4 + max_blocks * 4 + 64;
+  cudaError_t e = cudaSuccess;
+  auto chk = [&](cudaError_t x) { if (e == cudaSuccess) e = x; };
+  chk(cudaMalloc(&c->d_off, NM * 4));
+  chk(cudaMalloc(&c->d_cos, NM * half * 4));
+  chk(cudaMalloc(&c->d_sin, NM * half * 4));
+  chk(cudaMalloc(&c->d_tok_block, static_cast<size_t>(max_shared) * 4));
+  chk(cudaMalloc(&c->d_blk_start, static_cast<size_t>(max_blocks) * 4));
+  chk(cudaMalloc(&c->d_dev, NS * 4));
+  chk(cudaMalloc(&c->d_rank, NS * 4));
+  chk(cudaMalloc(&c->d_mask, static_cast<size_t>(max_agents) * nbw * 4));
+  chk(cudaMalloc(&c->d_cand, static_cast<size_t>(max_agents) * nbw * 4));
+  chk(cudaMalloc(&c->d_wprefix, (static_cast<size_t>(max_agents) * nbw + max_agents) * 4));
+  chk(cudaMalloc(&c->d_aprefix, (static_cast<size_t>(max_agents) + 1) * 8));
+  chk(cudaMalloc(&c->d_flag, static_cast<size_t>(max_agents) * s.n_layers * max_nb));
+  chk(cudaMalloc(&c->d_ints, 4 * sizeof(int32_t)));
+  chk(cudaMalloc(&c->d_bound, sizeof(int64_t)));
+  chk(cudaMalloc(&c->d_err, sizeof(uint32_t)));
+  chk(cudaMallocHost(&c->h_stage, c->stage_bytes));
+  chk(cudaMallocHost(&c->h_words, 4 * sizeof(int64_t)));
+  chk(cudaEventCreateWithFlags(&c->stage_done, cudaEventDisableTiming));
+  if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->d_ints, 0, 4 * sizeof(int32_t));
+  if (e != cudaSuccess) {
+    free_ctx(c);
+    return TD_ERR_CUDA;
+  }
+  *out = c;
+  return TD_OK;
+}
+
+td_status td_ctx_destroy(td_ctx* ctx) {
+  if (!ctx) return TD_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  free_ctx(ctx);
+  return TD_OK;
+}
+
+td_status td_round_offsets(const td_round* r, int32_t* off_out) {
+  if (!r || !off_out || !r->block_len || !r->hist_len || !r->perm || r->n_agents < 1 ||
+      r->n_blocks < 1)
+    return TD_ERR_INVALID_ARG;
+  const int N = r->n_agents, M = r->n_blocks;
+  for (int i = 0; i < N; ++i) {
+    std::vector<char> seen(M, 0);
+    int64_t pos = r->hist_len[i];
+    if (pos < 0) return TD_ERR_INVALID_ARG;
+    for (int q = 0; q < M; ++q) {
+      const int j = r->perm[static_cast<int64_t>(i) * M + q];
+      if (j < 0 || j >= M || seen[j] || r->block_len[j] < 1) return TD_ERR_INVALID_ARG;
+      seen[j] = 1;
+      if (pos > INT32_MAX) return TD_ERR_INVALID_ARG;
+      off_out[static_cast<int64_t>(i) * M + j] = static_cast<int32_t>(pos);
+      pos += r->block_len[j];
+    }
+  }
+  return TD_OK;
+}
+
+td_status td_rerotate_batched(td_ctx* c, const td_round* r, const void* k_canon,
+                              const void* v_canon, int32_t layer_begin, int32_t layer_end,
+                              const td_paged* pool, void* stream) {
+  if (!c || !same_device(c) || !k_canon || !aligned16(k_canon) ||
+      (v_canon && !aligned16(v_canon)))
+    return TD_ERR_INVALID_ARG;
+  if (layer_begin < 0 || layer_end > c->shape.n_layers || layer_begin > layer_end)
+    return TD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  td_status s = prepare_round(c, r, st);
+  if (s != TD_OK) return s;
+  PoolDev pd;
+  if ((s = pool_dev(c, r, pool, &pd)) != TD_OK) return s;
+  return cuda_status(launch_rerotate(c->g, round_dev(c), pd,
+                                     static_cast<const uint16_t*>(k_canon),
+                                     static_cast<const uint16_t*>(v_canon), layer_begin,
+                                     layer_end - layer_begin, c->d_err, st));
+}
+
+td_status td_check_select(td_ctx* c, const td_round* r, int32_t check_layer,
+                          const td_paged* pool, const void* k_fresh, int32_t recompute_pct,
+                          int32_t* sel, float* dev_out, int32_t* k_out, void* stream) {
+  if (!c || !same_device(c) || !k_fresh || !aligned16(k_fresh) || !k_out)
+    return TD_ERR_INVALID_ARG;
+  if (check_layer < 0 || check_layer >= c->shape.n_layers || recompute_pct < 0 ||
+      recompute_pct > 100)
+    return TD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  td_status s = prepare_round(c, r, st);
+  if (s != TD_OK) return s;
+  PoolDev pd;
+  if ((s = pool_dev(c, r, pool, &pd)) != TD_OK) return s;
+  const int k = static_cast<int>((static_cast<int64_t>(recompute_pct) * c->S + 99) / 100);
+  if (k > 0 && !sel) return TD_ERR_INVALID_ARG;
+  *k_out = k;
+  float* dev = dev_out ? dev_out : c->d_dev;
+  const RoundDev rd = round_dev(c);
+  cudaError_t e = launch_deviation(c->g, rd, pd, check_layer,
+                                   static_cast<const uint16_t*>(k_fresh), dev, c->d_err, st);
+  if (e == cudaSuccess) e = launch_select(dev, rd.N, rd.S, k, sel, st);
+  return cuda_status(e);
+}
+
+td_status td_pick_master(td_ctx* c, const td_round* r, const int32_t* sel, int32_t k,
+                         int64_t* cost_out, int32_t* master_dev, int32_t* master_host,
+                         void* stream) {
+  if (!c || !same_device(c) || !master_dev || k < 0 || (k > 0 && !sel))
+    return TD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  td_status s = prepare_round(c, r, st);
+  if (s != TD_OK) return s;
+  if (k > c->S) return TD_ERR_INVALID_ARG;
+  cudaError_t e = launch_pick_master(sel, c->N, c->S, k, cost_out, master_dev, c->d_err, st);
+  if (e != cudaSuccess) return TD_ERR_CUDA;
+  if (master_host) {
+    int32_t* h = reinterpret_cast<int32_t*>(c->h_words);
+    if ((e = cudaMemcpyAsync(h, master_dev, 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(st)) != cudaSuccess)
+      return TD_ERR_CUDA;
+    *master_host = *h;
+  }
+  return TD_OK;
+}
+
+td_status td_diff_encode(td_ctx* c, const td_round* r, const int32_t* master,
+                         const void* k_canon, const void* v_canon, const int32_t* sel,
+                         int32_t k, const void* k_fresh_sel, const void* v_fresh_sel,
+                         int32_t layer_begin, int32_t layer_end, td_diff_store* store,
+                         int64_t* nnz_out, void* stream) {
+  if (!c || !same_device(c) || !master || !k_canon || !v_canon || !store ||
+      !aligned16(k_canon) || !aligned16(v_canon))
+    return TD_ERR_INVALID_ARG;
+  if (k < 0 || (k > 0 && (!sel || !k_fresh_sel || !v_fresh_sel || !aligned16(k_fresh_sel) ||
+                          !aligned16(v_fresh_sel))))
+    return TD_ERR_INVALID_ARG;
+  if (layer_begin < 0 || layer_end > c->shape.n_layers || layer_begin >= layer_end)
+    return TD_ERR_INVALID_ARG;
+  if (!store->master_k || !store->master_v || !store->rowptr || !store->slot ||
+      !aligned16(store->master_k) || !aligned16(store->master_v) || store->capacity_blocks < 0)
+    return TD_ERR_INVALID_ARG;
+  if (store->capacity_blocks > 0 &&
+      (!store->block_idx || !store->val_k || !store->val_v || !aligned16(store->val_k) ||
+       !aligned16(store->val_v)))
+    return TD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  td_status s = prepare_round(c, r, st);
+  if (s != TD_OK) return s;
+  if (k > c->S) return TD_ERR_INVALID_ARG;
+  const int nl = layer_end - layer_begin;
+  StoreDev sd;
+  sd.master_k = static_cast<uint16_t*>(store->master_k);
+  sd.master_v = static_cast<uint16_t*>(store->master_v);
+  sd.rowptr = store->rowptr;
+  sd.block_idx = store->block_idx;
+  sd.val_k = static_cast<uint16_t*>(store->val_k);
+  sd.val_v = static_cast<uint16_t*>(store->val_v);
+  sd.slot = store->slot;
+  sd.capacity = store->capacity_blocks;
+  sd.nl = nl;
+  EncodeScratch sc;
+  sc.rank = c->d_rank;
+  sc.mask = c->d_mask;
+  sc.cand = c->d_cand;
+  sc.word_prefix = c->d_wprefix;
+  sc.agent_prefix = c->d_aprefix;
+  sc.flag = c->d_flag;
+  sc.need_fixup = c->d_ints;
+  sc.nbw = (((c->S + kDiffBlock - 1) / kDiffBlock) + 31) / 32;
+  cudaError_t e = launch_encode(c->g, round_dev(c), master,
+                                static_cast<const uint16_t*>(k_canon),
+                                static_cast<const uint16_t*>(v_canon), sel, k,
+                                static_cast<const uint16_t*>(k_fresh_sel),
+                                static_cast<const uint16_t*>(v_fresh_sel), nl, sd, sc, c->d_err,
+                                c->d_bound, st);
+  if (e != cudaSuccess) return TD_ERR_CUDA;
+  store->layer_begin = layer_begin;
+  store->layer_end = layer_end;
+  if (nnz_out) {
+    int64_t* h = c->h_words;
+    if (cudaMemcpyAsync(h, c->d_bound, 8, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(h + 1, store->rowptr + static_cast<int64_t>(c->N) * nl, 8,
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return TD_ERR_CUDA;
+    if (h[0] > store->capacity_blocks) {
+      *nnz_out = h[0];
+      return TD_ERR_CAPACITY;
+    }
+    *nnz_out = h[1];
+  }
+  return TD_OK;
+}
+
+td_status td_fused_restore(td_ctx* c, const td_round* r, const td_diff_store* store,
+                           const int32_t* agents, int32_t n_list, int32_t layer_begin,
+                           int32_t layer_end, int32_t frame, const td_paged* pool,
+                           void* stream) {
+  if (!c || !same_device(c) || !store || (n_list > 0 && !agents) || n_list < 0 ||
+      (frame != 0 && frame != 1))
+    return TD_ERR_INVALID_ARG;
+  if (!store->master_k || !store->master_v || !store->slot || !aligned16(store->master_k) ||
+      !aligned16(store->master_v))
+    return TD_ERR_INVALID_ARG;
+  if (layer_begin < store->layer_begin || layer_end > store->layer_end ||
+      layer_begin >= layer_end || store->layer_begin < 0 ||
+      store->layer_end > c->shape.n_layers)
+    return TD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  td_status s = prepare_round(c, r, st);
+  if (s != TD_OK) return s;
+  for (int x = 0; x < n_list; ++x)
+    if (agents[x] < 0 || agents[x] >= c->N) return TD_ERR_INVALID_ARG;
+  PoolDev pd;
+  if ((s = pool_dev(c, r, pool, &pd)) != TD_OK) return s;
+  StoreDev sd;
+  sd.master_k = static_cast<uint16_t*>(store->master_k);
+  sd.master_v = static_cast<uint16_t*>(store->master_v);
+  sd.rowptr = store->rowptr;
+  sd.block_idx = store->block_idx;
+  sd.val_k = static_cast<uint16_t*>(store->val_k);
+  sd.val_v = static_cast<uint16_t*>(store->val_v);
+  sd.slot = store->slot;
+  sd.capacity = store->capacity_blocks;
+  sd.nl = store->layer_end - store->layer_begin;
+  const RoundDev rd = round_dev(c);
+  for (int x0 = 0; x0 < n_list; x0 += kMaxListAgents) {
+    AgentList al;
+    al.n = n_list - x0 < kMaxListAgents ? n_list - x0 : kMaxListAgents;
+    for (int x = 0; x < al.n; ++x) al.a[x] = agents[x0 + x];
+    cudaError_t e = launch_restore(c->g, rd, pd, sd, al, layer_begin, store->layer_begin,
+                                   layer_end - layer_begin, frame, c->d_err, st);
+    if (e != cudaSuccess) return TD_ERR_CUDA;
+  }
+  return TD_OK;
+}
+
+td_status td_get_error(td_ctx* c, void* stream, uint32_t* bits_out) {
+  if (!c || !same_device(c)) return TD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* h = reinterpret_cast<uint32_t*>(c->h_words);
+  if (cudaMemcpyAsync(h, c->d_err, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(c->d_err, 0, 4, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return TD_ERR_CUDA;
+  const uint32_t bits = *h;
+  if (bits_out) *bits_out = bits;
+  for (int code = 1; code < 32; ++code)
+    if (bits & (1u << code)) return static_cast<td_status>(code);
+  return TD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// td_internal.h - types shared by the host layer (td_host.cpp) and the kernels (*.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "td.h"
+
+#ifdef __CUDACC__
+#define TD_HD __host__ __device__
+#else
+#define TD_HD
+#endif
+
+namespace td {
+
+constexpr int kDiffBlock = 16;     // tokens per diff block (canonical axis)
+constexpr int kMaxListAgents = 256; // agents per restore launch (passed by value)
+
+TD_HD inline uint32_t err_bit(td_status s) { return 1u << static_cast<uint32_t>(s); }
+
+// Token geometry of one model shape.
+struct Geom {
+  int H, D, E;   // heads, head_dim, elements per token row
+  int half;      // D / 2
+  int vpt;       // pair-vectors per token = E / 16 (8 frequencies of one head each)
+};
+
+// The current round's device tables (owned by the context).
+struct RoundDev {
+  int N, M, S, nb;
+  const int32_t* off;        // [N*M] block start in each agent's prompt
+  const float* cos_t;        // [N*M][D/2] cos of off * theta^(-2f/D), rounded to float
+  const float* sin_t;        // [N*M][D/2]
+  const int32_t* tok_block;  // [S] block of each canonical token
+  const int32_t* blk_start;  // [M] canonical start of each block
+};
+
+struct PoolDev {
+  uint16_t* base;            // [L][2][num_pages][P][E]
+  int64_t num_pages;
+  const int32_t* bt;         // [N][max_lp]
+  int max_lp;
+  int P;
+  int p_shift;               // log2(P) when P is a power of two, else -1
+};
+
+struct AgentList {
+  int n;
+  int32_t a[kMaxListAgents];
+};
+
+// Per-launch view of a diff store (offsets already relative to its first layer).
+struct StoreDev {
+  uint16_t* master_k;
+  uint16_t* master_v;
+  int64_t* rowptr;
+  int32_t* block_idx;
+  uint16_t* val_k;
+  uint16_t* val_v;
+  int32_t* slot;
+  int64_t capacity;
+  int nl;                    // layers held by the store
+};
+
+// Encode scratch (owned by the context).
+struct EncodeScratch {
+  int32_t* rank;             // [N][S] index of t in sel_i, or -1
+  uint32_t* mask;            // [N][nbw] blocks holding a selected token of agent i
+  uint32_t* cand;            // [N][nbw] mask_i | mask_m for i != m, 0 for the master
+  int32_t* word_prefix;      // [N][nbw] candidates of agent i in words before w
+  int64_t* agent_prefix;     // [N+1] candidates per layer of agents before i
+  uint8_t* flag;             // [N][nl][nb] candidate block differs from the master's
+  int32_t* need_fixup;       // 1 when some candidate equalled the master's block
+  int nbw;
+};
+
+int tile_threads(const Geom& g);
+
+cudaError_t launch_rerotate(const Geom& g, const RoundDev& rd, const PoolDev& pool,
+                            const uint16_t* kc, const uint16_t* vc, int layer_begin, int nl,
+                            uint32_t* err, cudaStream_t st);
+
+cudaError_t launch_deviation(const Geom& g, const RoundDev& rd, const PoolDev& pool,
+                             int check_layer, const uint16_t* k_fresh, float* dev,
+                             uint32_t* err, cudaStream_t st);
+
+cudaError_t launch_select(const float* dev, int N, int S, int k, int32_t* sel,
+                          cudaStream_t st);
+
+cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int k, int64_t* cost,
+                               int32_t* master, uint32_t* err, cudaStream_t st);
+
+cudaError_t launch_encode(const Geom& g, const RoundDev& rd, const int32_t* master,
+                          const uint16_t* kc, const uint16_t* vc, const int32_t* sel, int k,
+                          const uint16_t* kf, const uint16_t* vf, int nl,
+                          const StoreDev& store, const EncodeScratch& sc, uint32_t* err,
+                          int64_t* bound_dev, cudaStream_t st);
+
+cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& pool,
+                           const StoreDev& store, const AgentList& agents, int layer_begin,
+                           int store_layer0, int nl, int frame, uint32_t* err,
+                           cudaStream_t st);
+
+}  // namespace td

@@ -1,0 +1,221 @@
+/*
+ * td.h - C ABI of the collective KV cache path on GB300 (sm_103a).
+ *
+ * The path is the data-parallel core of TokenDance ("TokenDance: Scaling Multi-Agent LLM
+ * Serving via Collective KV Cache Sharing", arXiv 2604.03143), as described by the
+ * structured review at zhaifeiyue.github.io/papers/2604.03143/detail.html (cited as [R])
+ * and the juhe.plus blog post on the paper (cited as [B]). One All-Gather round: N agents
+ * share M output blocks; agent i sees its private history H_i followed by the blocks in
+ * its own order Pi_i ([R] Summary, Motivation; Figure 1). Four stages:
+ *   1 td_rerotate_batched  one launch turns the shared blocks' canonical-frame K to every
+ *                          agent's offsets and writes all agents' paged KV
+ *   2 td_check_select      one key-deviation pass at the check layer picks each agent's
+ *                          important (to be recomputed) positions
+ *   3 td_pick_master       picks the Master agent;
+ *     td_diff_encode       stores the Master dense and every other agent (Mirror) as
+ *                          block-sparse K/V diffs
+ *   4 td_fused_restore     gathers the Master, merges each agent's diffs, turns K back to
+ *                          the agent's offsets and writes its paged KV; no dense Mirror
+ *
+ * Conventions for every call
+ *   - Device pointers are CUDA device addresses of the current device; host pointers are
+ *     ordinary host memory. Each argument says which it is. All memory is owned by the
+ *     caller except the context's private workspace.
+ *   - bf16 tensors are raw 16-bit patterns, row-major. E = n_kv_heads * head_dim.
+ *   - S = sum of block_len (shared tokens). nb = ceil(S / 16) diff blocks.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t) unless stated otherwise. Calls
+ *     that share a context must be ordered (one stream, or the caller's events).
+ *   - Host validation runs first; an invalid argument returns TD_ERR_INVALID_ARG and
+ *     launches nothing. A CUDA launch or copy failure returns TD_ERR_CUDA.
+ *   - Faults found on the device never trap: the offending write is skipped and a bit
+ *     is set in the context's error word, read and cleared by td_get_error.
+ *   - Every output is a deterministic function of the inputs.
+ */
+#ifndef TD_H
+#define TD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum td_status {
+  TD_OK = 0,
+  TD_ERR_INVALID_ARG = 1,    /* bad shape, pointer, range or size; nothing launched */
+  TD_ERR_CUDA = 2,           /* a CUDA runtime call failed */
+  TD_ERR_CAPACITY = 3,       /* diff store too small (see td_diff_encode) */
+  TD_ERR_UNMAPPED_PAGE = 4,  /* a block-table entry was -1 or >= num_pages */
+  TD_ERR_NONFINITE = 5,      /* a key deviation was NaN or infinite */
+  TD_ERR_DEVICE_TIMEOUT = 6  /* reserved: no kernel of this library waits on another */
+} td_status;
+
+/* Model shape. head_dim must be a multiple of 16 (RoPE pairs element f with f + D/2 and
+ * the kernels move 8 elements per 16-byte vector); diff_block must be 16. */
+typedef struct td_shape {
+  int32_t n_layers;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;    /* tokens per KV page, >= 1 */
+  int32_t diff_block;   /* tokens per diff block on the canonical axis: 16 */
+  double rope_theta;    /* RoPE base, e.g. 1e6 for Qwen2.5 */
+} td_shape;
+
+/* One All-Gather round ([R] Summary, Motivation: P_i = H_i || Pi_i(O); Figure 1).
+ * All arrays are HOST memory, read during the call only. Block j's offset in agent i's
+ * prompt is hist_len[i] plus the lengths of the blocks that perm[i] places before j. */
+typedef struct td_round {
+  int32_t n_agents;          /* N >= 1 */
+  int32_t n_blocks;          /* M >= 1 */
+  const int32_t* block_len;  /* [M] host, each >= 1 */
+  const int32_t* hist_len;   /* [N] host, each >= 0 */
+  const int32_t* perm;       /* [N*M] host; perm[i*M+q] = block at slot q of agent i */
+} td_round;
+
+/* Paged KV cache shared by all agents ([R] §3d, §5: vLLM paged KV with block tables).
+ * base: DEVICE, bf16, layout [L][2][num_pages][page_size][H][D] (index 0 = K, 1 = V).
+ * block_table: DEVICE int32 [N][max_pages_per_agent]; entry = physical page of the
+ * agent's logical page, -1 = unmapped. The token at prompt position p of agent i lives in
+ * page block_table[i][p / page_size], slot p % page_size. Only positions of the shared
+ * span are written; pages holding only history may stay unmapped. */
+typedef struct td_paged {
+  void* base;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int32_t max_pages_per_agent;
+} td_paged;
+
+/* Master-Mirror diff store ([R] Summary Method (3); Figure 8; §2b item 2: one
+ * (indices, values) record per Mirror per layer). All pointers DEVICE, caller-allocated.
+ * It covers the layers [layer_begin, layer_end) it was encoded for; nl = their count.
+ * K is kept in the canonical frame (block-local RoPE positions).
+ *   master_k, master_v  bf16 [nl][S][E]       the Master's cache, dense
+ *   rowptr              int64 [N*nl + 1]      CSR rows, row = agent*nl + (layer-layer_begin)
+ *   block_idx           int32 [capacity]      diff block index b of each record, ascending
+ *                                             within a row
+ *   val_k, val_v        bf16 [capacity][16][E] the Mirror's whole block; tokens past S are 0
+ *   slot                int32 [N*nl*nb]       record of (agent, layer, block), or -1
+ *   capacity_blocks     records the value arrays can hold
+ * The Master's rows are empty. */
+typedef struct td_diff_store {
+  void* master_k;
+  void* master_v;
+  int64_t* rowptr;
+  int32_t* block_idx;
+  void* val_k;
+  void* val_v;
+  int32_t* slot;
+  int64_t capacity_blocks;
+  int32_t layer_begin;   /* written by td_diff_encode */
+  int32_t layer_end;     /* written by td_diff_encode */
+} td_diff_store;
+
+typedef struct td_ctx td_ctx;
+
+/* Create a context for one model shape. It owns only scratch space: the round's offset
+ * and RoPE tables, the per-agent rank and mask tables, the deviations when the caller
+ * does not keep them, the encode flags, and the error word. Limits: N <= max_agents,
+ * M <= max_blocks, S <= max_shared. Uses the current CUDA device. Synchronous. */
+td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_blocks,
+                        int32_t max_shared, td_ctx** out);
+td_status td_ctx_destroy(td_ctx* ctx);
+
+/* Static text for a status code. */
+const char* td_status_string(td_status s);
+
+/* Block offsets of a round (host only): off_out[i*M + j] = prompt position where block j
+ * starts in agent i ([R] Summary, Motivation; Figure 1). off_out: HOST int32 [N*M]. */
+td_status td_round_offsets(const td_round* round, int32_t* off_out);
+
+/* Stage 1 - collective re-rotation ([R] Summary Method (2): the round's requests are
+ * batched and RoPE runs once for the group; Figure 7 T3; §2a "Collective prefill").
+ * For every agent i, layer l in [layer_begin, layer_end) and shared token t of block j at
+ * local index u: pool K of agent i at position off_ij + u = bf16(R(off_ij) Kc[l][t]) and,
+ * when v_canon is not NULL, pool V there = Vc[l][t]. RoPE: neox pairing (f, f + D/2),
+ * angle off * theta^(-2f/D), cos/sin computed in float64 on the host and rounded to float;
+ * y0 = fma(x0, c, -(x1*s)), y1 = fma(x1, c, x0*s) in float32, rounded to bf16 (nearest
+ * even). k_canon, v_canon: DEVICE bf16 [layer_end-layer_begin][S][E] (row 0 = layer
+ * layer_begin). Canonical frame: block j's K rotated as if the block started at 0. */
+td_status td_rerotate_batched(td_ctx* ctx, const td_round* round, const void* k_canon,
+                              const void* v_canon, int32_t layer_begin, int32_t layer_end,
+                              const td_paged* pool, void* stream);
+
+/* Stage 2 - key deviation at the check layer and per-agent top-k ([R] Summary Method (2):
+ * one key-difference analysis at the check layer, whose important positions all later
+ * layers reuse; §3c A3). dev_i(t) = sum over the E elements of (fresh - reused)^2 in
+ * float32, summed in a fixed order (16-byte vector v -> lane v mod 32, lanes ascending
+ * through their vectors with fma, then a pairwise tree over the 32 lanes). reused = pool K
+ * of agent i at its position of t, layer check_layer. k = ceil(recompute_pct * S / 100);
+ * sel_i = the k tokens of largest dev (ties to the lower token), ascending.
+ *   k_fresh  DEVICE bf16 [N][S][E]   recomputed K at the check layer, agent frame,
+ *                                    canonical token order
+ *   sel      DEVICE int32 [N][k]     output
+ *   dev_out  DEVICE float [N][S]     output, or NULL
+ *   k_out    HOST int32              k (computed on the host; no sync)
+ * A non-finite deviation sets TD_ERR_NONFINITE in the error word (selection undefined). */
+td_status td_check_select(td_ctx* ctx, const td_round* round, int32_t check_layer,
+                          const td_paged* pool, const void* k_fresh, int32_t recompute_pct,
+                          int32_t* sel, float* dev_out, int32_t* k_out, void* stream);
+
+/* Stage 3a - Master choice ([R] Summary Method (3): keep the agent with the smallest
+ * deviation dense; §3c A2: chosen by a deviation score so the diffs are sparsest).
+ * mask_i = diff blocks (16 tokens) holding a token of sel_i; cost(m) = sum over i != m of
+ * |mask_i OR mask_m| (the number of diff blocks per layer the Mirrors can need);
+ * master = argmin, ties to the lower index.
+ *   sel          DEVICE int32 [N][k]
+ *   cost_out     DEVICE int64 [N], or NULL
+ *   master_dev   DEVICE int32, output (read by td_diff_encode)
+ *   master_host  HOST int32, or NULL; when given the call synchronizes the stream */
+td_status td_pick_master(td_ctx* ctx, const td_round* round, const int32_t* sel, int32_t k,
+                         int64_t* cost_out, int32_t* master_dev, int32_t* master_host,
+                         void* stream);
+
+/* Stage 3b - Master-Mirror block-sparse encoding ([R] Summary Method (3): Master keeps a
+ * full cache, every other agent records only the indices and values of its differing
+ * blocks; Figure 8; §2a "Diff serialize: Mirror dense -> (indices, K/V)"). Agent i's
+ * canonical cache X_i(t) is its recomputed K turned back by R(-off) (same float32 / bf16
+ * rounding as stage 1, with the signs of R(-a)) and recomputed V at t in sel_i, and the
+ * canonical K/V elsewhere. The store receives X_master densely and, for each Mirror i,
+ * layer and diff block b in ascending order, X_i's block b when any K or V bit of the
+ * block differs from X_master's. No Mirror is ever materialised densely.
+ *   master       DEVICE int32 (as written by td_pick_master, or the caller's choice)
+ *   k_canon, v_canon   DEVICE bf16 [nl][S][E], row 0 = layer layer_begin
+ *   sel          DEVICE int32 [N][k], each row ascending, as td_check_select writes it
+ *   k_fresh_sel, v_fresh_sel  DEVICE bf16 [N][nl][k][E]: recomputed K (agent frame) and V
+ *                of sel[i][r] at layer layer_begin + l in row [i][l][r]
+ *   store        caller-allocated; capacity_blocks must be at least the candidate bound
+ *                nl * cost(master) (cost as td_pick_master defines it), because blocks
+ *                are first written at positions derived from the masks
+ *   nnz_out      HOST int64, or NULL. When given, the call synchronizes the stream and
+ *                returns TD_ERR_CAPACITY if the bound exceeds the capacity (then
+ *                *nnz_out = the bound); otherwise *nnz_out = records written.
+ * When the bound exceeds the capacity only master_k/master_v and rowptr are written and
+ * TD_ERR_CAPACITY is also set in the error word. */
+td_status td_diff_encode(td_ctx* ctx, const td_round* round, const int32_t* master,
+                         const void* k_canon, const void* v_canon, const int32_t* sel,
+                         int32_t k, const void* k_fresh_sel, const void* v_fresh_sel,
+                         int32_t layer_begin, int32_t layer_end, td_diff_store* store,
+                         int64_t* nnz_out, void* stream);
+
+/* Stage 4 - fused diff restore ([R] Summary Method (3): on read-back the diffs are merged
+ * into the Master's data in flight and RoPE is recovered, with no dense Mirror; §2a
+ * "Fused restore: Master chunk + diff -> paged KV"; §3d). For each listed agent a, layer
+ * l in [layer_begin, layer_end) (inside the store's range) and token t: source = a's
+ * diff record for (l, t / 16) if present, else the Master; pool K at a's position of t =
+ * bf16(R(off) source K) when frame == 0, or source K unchanged when frame == 1; pool V =
+ * source V. Rounding as in stage 1.
+ *   agents  HOST int32 [n_list], each in [0, N) */
+td_status td_fused_restore(td_ctx* ctx, const td_round* round, const td_diff_store* store,
+                           const int32_t* agents, int32_t n_list, int32_t layer_begin,
+                           int32_t layer_end, int32_t frame, const td_paged* pool,
+                           void* stream);
+
+/* Synchronize the stream, read and clear the error word. Returns TD_OK when no device
+ * fault was recorded, else the lowest td_status code recorded; bits_out (HOST, or NULL)
+ * receives the whole word (bit c set = code c recorded). */
+td_status td_get_error(td_ctx* ctx, void* stream, uint32_t* bits_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TD_H */
