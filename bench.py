@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 METRIC = "restore+reuse KV GB/s (% of GB300 HBM peak); agent-rounds/sec, 7B shape"
 UNIT = "GB/s"
 LAUNCHES_PER_STEP = 11   # rerotate 1, deviation+select 2, master 1, encode 6, restore 1
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -104,7 +104,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu, f"--query-gpu={CLOCK_FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -121,28 +121,42 @@ class ClockSampler:
                 self.proc.kill()
                 self.out = ""
 
+    def mark(self, name):
+        setattr(self, name, time.time())
+
     def summary(self):
+        """Median SM clock and throttle reasons over the samples taken while our steps ran
+        (warm-up and timed steps; the timed region alone is often shorter than the
+        sampling period)."""
         if not self.proc:
             return None
-        sm, mx, reasons = [], [], set()
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                 "sw_power_cap"]
+        rows = []
         for line in (self.out or "").strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
+            except (ValueError, IndexError):
                 continue
-            for name, val in zip(names[1:], f[5:9]):
+        t0 = getattr(self, "load_start", None)
+        t1 = getattr(self, "load_end", None)
+        under = [r for r in rows if t0 is None or (t0 - 0.05 <= r[0] <= (t1 or 1e18) + 0.05)]
+        if not under:
+            under = rows
+        if not under:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in under:
+            for name, val in zip(names, r[3]):
                 if val.lower() in ("active", "0x1", "1"):
                     reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(r[1] for r in under),
+                "sm_max_mhz": max(r[2] for r in under), "reasons": sorted(reasons),
+                "samples": len(under), "window": "warm-up and timed steps"}
 
 
 # ------------------------------------------------------------------ our arm
@@ -237,6 +251,10 @@ def bench_ours(args, rank, world, local_rank):
     agents = list(range(cfg.n_agents))
     N, L = cfg.n_agents, cfg.n_layers
 
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] \
+        if world == 1 else str(local_rank)
+    clk = ClockSampler(gpu_id if gpu_id.isdigit() else "0").__enter__()
+    clk.mark("load_start")
     for _ in range(args.warmup):
         run_step(st, agents)
     torch.cuda.synchronize()
@@ -247,17 +265,16 @@ def bench_ours(args, rank, world, local_rank):
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0] \
-        if world == 1 else str(local_rank)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(gpu_id if gpu_id.isdigit() else "0") as clk:
-        start.record(rr.stream)
-        for i in range(K):
-            run_step(st, agents, evs[i])
-        end.record(rr.stream)
-        torch.cuda.synchronize()
+    start.record(rr.stream)
+    for i in range(K):
+        run_step(st, agents, evs[i])
+    end.record(rr.stream)
+    torch.cuda.synchronize()
+    clk.mark("load_end")
+    clk.__exit__(None, None, None)
     if world > 1:
         dist.barrier()
     ms_total = start.elapsed_time(end)
@@ -411,16 +428,23 @@ def oracle_step(sub, rnd, kc, vc, orc, cache):
     return secs, sel.shape[1], store["nnz"]
 
 
-def cpu_baseline(cfg, seed, layers):
+def cpu_baseline(cfg, seed, layers=None, min_seconds=10.0, max_passes=8):
+    """The oracle, single-threaded, on the same round (all layers unless `layers`),
+    repeated until at least `min_seconds` of oracle time have accumulated."""
+    layers = cfg.n_layers if layers is None else layers
     sub, rnd, kc, vc, orc = oracle_round(cfg, seed, layers)
     cache = {}
-    secs, k, nnz = oracle_step(sub, rnd, kc, vc, orc, cache)
-    by = sum(stage_bytes(sub, sub.n_agents, layers, k, nnz, sub.n_agents).values())
+    secs, passes, k, nnz = 0.0, 0, 0, 0
+    while passes < max_passes and (passes == 0 or secs < min_seconds):
+        t, k, nnz = oracle_step(sub, rnd, kc, vc, orc, cache)
+        secs += t
+        passes += 1
+    by = sum(stage_bytes(sub, sub.n_agents, layers, k, nnz, sub.n_agents).values()) * passes
     return {"value": round(by / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "seconds": round(secs, 2),
-            "sample": f"the same round restricted to layers 0..{layers - 1} of {cfg.n_layers} "
-                      f"(all {cfg.n_agents} agents, all {cfg.n_shared} shared tokens), one "
-                      f"single-threaded pass of the plain C oracle"}
+            "sample": f"{passes} single-threaded passes of the plain C oracle over the same "
+                      f"round, layers 0..{layers - 1} of {cfg.n_layers} (all {cfg.n_agents} "
+                      f"agents, all {cfg.n_shared} shared tokens)"}
 
 
 def bench_reference(args, rank, world):
@@ -467,7 +491,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen7b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-layers", type=int, default=12)
+    ap.add_argument("--cpu-layers", type=int, default=None)
     ap.add_argument("--ref-layers", type=int, default=4)
     args = ap.parse_args(argv)
     if args.warmup < 3:
