@@ -26,7 +26,8 @@ CU_FLAGS = ["-O3", "-lineinfo", "--fmad=false", "-std=c++17", "-Xcompiler", "-fP
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", "-fno-fast-math", "-Wall",
              "-Wextra"]
 
-CU_SOURCES = ["k_rerotate.cu", "k_select.cu", "k_master.cu", "k_encode.cu", "k_restore.cu"]
+CU_SOURCES = ["k_rerotate.cu", "k_select.cu", "k_master.cu", "k_encode.cu", "k_restore.cu",
+              "td_noalloc.cu"]
 CXX_SOURCES = ["td_host.cpp"]
 HEADERS = ["td_internal.h", "td_device.cuh"]
 

@@ -224,6 +224,7 @@ const char* td_status_string(td_status s) {
     case TD_ERR_UNMAPPED_PAGE: return "unmapped or out-of-range page";
     case TD_ERR_NONFINITE: return "non-finite key deviation";
     case TD_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case TD_ERR_SCRATCH_LIMIT: return "round exceeds the fixed scratch of td_check_select_noalloc";
   }
   return "unknown status";
 }

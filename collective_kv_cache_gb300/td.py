@@ -25,6 +25,7 @@ TD_ERR_CAPACITY = 3
 TD_ERR_UNMAPPED_PAGE = 4
 TD_ERR_NONFINITE = 5
 TD_ERR_DEVICE_TIMEOUT = 6
+TD_ERR_SCRATCH_LIMIT = 7
 
 
 class td_shape(C.Structure):
@@ -75,6 +76,8 @@ def _load() -> C.CDLL:
         "td_fused_restore": [VP, P(td_round), P(td_diff_store), VP, I32, I32, I32, I32,
                              P(td_paged), VP],
         "td_get_error": [VP, VP, P(C.c_uint32)],
+        "td_check_select_noalloc": [P(td_shape), P(td_round), I32, P(td_paged), VP, I32, VP,
+                                    P(I32), P(C.c_uint32), VP],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -88,7 +91,7 @@ def _load() -> C.CDLL:
 _lib = _load()
 EXPORTS = ("td_ctx_create", "td_ctx_destroy", "td_status_string", "td_round_offsets",
            "td_rerotate_batched", "td_check_select", "td_pick_master", "td_diff_encode",
-           "td_fused_restore", "td_get_error")
+           "td_fused_restore", "td_get_error", "td_check_select_noalloc")
 
 
 def lib_path() -> str:
@@ -170,6 +173,17 @@ def td_fused_restore(ctx, rnd, store: td_diff_store, agents: Sequence[int], laye
     s = _lib.td_fused_restore(ctx, C.byref(rnd), C.byref(store), ag.ctypes.data, len(ag),
                               layer_begin, layer_end, frame, C.byref(pool), stream)
     return _check(s, "td_fused_restore") if check else s
+
+
+def td_check_select_noalloc(shape: td_shape, rnd: td_round, check_layer, pool, k_fresh,
+                            recompute_pct, sel, stream=0, want_bits=True):
+    """Returns (status, k, error bits). Allocates nothing on the device."""
+    k = C.c_int32(0)
+    bits = C.c_uint32(0)
+    s = _lib.td_check_select_noalloc(C.byref(shape), C.byref(rnd), check_layer, C.byref(pool),
+                                     k_fresh, recompute_pct, sel, C.byref(k),
+                                     C.byref(bits) if want_bits else None, stream)
+    return s, k.value, bits.value
 
 
 def td_get_error(ctx, stream=0):

@@ -47,7 +47,8 @@ typedef enum td_status {
   TD_ERR_CAPACITY = 3,       /* diff store too small (see td_diff_encode) */
   TD_ERR_UNMAPPED_PAGE = 4,  /* a block-table entry was -1 or >= num_pages */
   TD_ERR_NONFINITE = 5,      /* a key deviation was NaN or infinite */
-  TD_ERR_DEVICE_TIMEOUT = 6  /* reserved: no kernel of this library waits on another */
+  TD_ERR_DEVICE_TIMEOUT = 6, /* reserved: no kernel of this library waits on another */
+  TD_ERR_SCRATCH_LIMIT = 7   /* sizes exceed the fixed scratch of td_check_select_noalloc */
 } td_status;
 
 /* Model shape. head_dim must be a multiple of 16 (RoPE pairs element f with f + D/2 and
@@ -209,6 +210,30 @@ td_status td_fused_restore(td_ctx* ctx, const td_round* round, const td_diff_sto
                            const int32_t* agents, int32_t n_list, int32_t layer_begin,
                            int32_t layer_end, int32_t frame, const td_paged* pool,
                            void* stream);
+
+/* td_check_select without a context and without any device allocation. The paper has
+ * no counterpart: this entry point exists for callers that may not call cudaMalloc (for
+ * instance code that runs under a pool allocator that forbids it, or inside a process
+ * whose device footprint must stay fixed after start-up). It computes exactly what
+ * td_check_select computes (same kernels, same order of summation, same selection).
+ * Its scratch - a copy of the round descriptor, the offset and token tables, the N*S
+ * deviations and an error word - is one fixed array in device memory (about 4.5 MiB),
+ * held by every GPU that loads the library until the process exits.
+ * Limits: N <= 256, M <= 256, N*M <= 16384, S <= 65536, N*S <= 1048576; larger rounds
+ * return TD_ERR_SCRATCH_LIMIT before anything is launched.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture. Every call
+ * reuses the same array: calls whose work can overlap on the GPU (different streams
+ * without ordering between them, or several host threads) race on it and must be
+ * serialized by the caller. The error word is cleared at the start of each call.
+ *   shape, round  HOST, as for td_ctx_create / td_check_select
+ *   pool, k_fresh, sel, k_out, check_layer, recompute_pct   as for td_check_select
+ *   err_bits_out  HOST, or NULL; when given the call synchronizes the stream, stores the
+ *                 device error word there and returns the lowest error code recorded */
+td_status td_check_select_noalloc(const td_shape* shape, const td_round* round,
+                                  int32_t check_layer, const td_paged* pool,
+                                  const void* k_fresh, int32_t recompute_pct, int32_t* sel,
+                                  int32_t* k_out, uint32_t* err_bits_out, void* stream);
 
 /* Synchronize the stream, read and clear the error word. Returns TD_OK when no device
  * fault was recorded, else the lowest td_status code recorded; bits_out (HOST, or NULL)
