@@ -245,6 +245,8 @@ def bench_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     cfg = synth.CONFIGS[args.workload]()
+    if args.layers:
+        cfg = cfg.replace(n_layers=args.layers, name=f"{cfg.name}_first{args.layers}layers")
     seed = rank_seed(cfg.seed, rank)
     st = setup_round(cfg, seed, device)
     rr = st["rr"]
@@ -489,6 +491,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="qwen7b")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="same shape with fewer layers (small profiling case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-layers", type=int, default=None)
