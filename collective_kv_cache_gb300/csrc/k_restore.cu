@@ -3,33 +3,34 @@
 // without building a dense Mirror; §2a "Fused restore: Master chunk + diff -> paged KV";
 // §3d: recovery belongs in the transfer path, written through the paged-KV slot map).
 //
-// One CTA per tile = (layer, one 16-token diff block). The Master's tile is read from HBM
-// once and held in registers; for each listed agent the slot map says whether that agent
-// has a record for this (layer, block): if so its record replaces the Master's tile for
-// this agent only. K is turned by the agent's block offsets (frame 0) or copied (frame 1),
-// V is copied, both stored 16 bytes per thread into the agent's page.
+// One CTA per unit = (layer, one 16-token diff block, K or V, part). The Master's data of
+// the unit is read from HBM once and held in registers; for each listed agent the slot
+// map says whether that agent has a record for this (layer, block): if so its record
+// replaces the Master's data for this agent only. K is turned by the agent's block
+// offsets (frame 0) or copied (frame 1), V is copied; 16-byte stores into the agent's
+// page.
 #include "td_device.cuh"
 
 namespace td {
 
 template <int kItems, bool kRotate>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agents,
                int layer_begin, int store_layer0, int tiles_per_layer, uint32_t* err) {
-  const int tile = blockIdx.x;
-  const int li = tile / tiles_per_layer;            // layer index within this call
-  const int b = tile - li * tiles_per_layer;
-  const int t0 = b * kDiffBlock;
-  const int layer = layer_begin + li;
+  const Unit un = unit_of(g, blockIdx.x, tiles_per_layer);
+  const int t0 = un.b * kDiffBlock;
+  const int layer = layer_begin + un.li;
   const int sl = layer - store_layer0;              // layer index within the store
   const int n_items = kDiffBlock * g.vpt;
+  const uint16_t* master = un.kv == 0 ? store.master_k : store.master_v;
+  const uint16_t* vals = un.kv == 0 ? store.val_k : store.val_v;
 
-  uint4 ka[kItems], kb[kItems], va[kItems], vb[kItems];
+  uint4 ma[kItems], mb[kItems];
   int e0[kItems], f0[kItems], tl[kItems], blk[kItems], u[kItems];
   bool live[kItems];
 #pragma unroll
   for (int r = 0; r < kItems; ++r) {
-    const int q = threadIdx.x + r * blockDim.x;
+    const int q = un.q0 + threadIdx.x + r * blockDim.x;
     const Item it = item_of(g, q < n_items ? q : 0);
     const int t = t0 + it.tok;
     live[r] = q < n_items && t < rd.S;
@@ -40,10 +41,8 @@ restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agen
     u[r] = 0;
     if (live[r]) {
       const int64_t row = (static_cast<int64_t>(sl) * rd.S + t) * g.E;
-      ka[r] = ldg16(store.master_k + row + it.e0);
-      kb[r] = ldg16(store.master_k + row + it.e0 + g.half);
-      va[r] = ldg16(store.master_v + row + it.e0);
-      vb[r] = ldg16(store.master_v + row + it.e0 + g.half);
+      ma[r] = ldg16(master + row + it.e0);
+      mb[r] = ldg16(master + row + it.e0 + g.half);
       blk[r] = __ldg(rd.tok_block + t);
       u[r] = t - __ldg(rd.blk_start + blk[r]);
     }
@@ -51,7 +50,7 @@ restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agen
 
   for (int x = 0; x < agents.n; ++x) {
     const int a = agents.a[x];
-    int rec = __ldg(store.slot + (static_cast<int64_t>(a) * store.nl + sl) * rd.nb + b);
+    const int rec = __ldg(store.slot + (static_cast<int64_t>(a) * store.nl + sl) * rd.nb + un.b);
     if (rec >= store.capacity) {  // a slot map that does not belong to this store
       if (threadIdx.x == 0) atomicOr(err, err_bit(TD_ERR_INVALID_ARG));
       continue;
@@ -59,30 +58,25 @@ restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agen
 #pragma unroll
     for (int r = 0; r < kItems; ++r) {
       if (!live[r]) continue;
-      uint4 sa = ka[r], sb = kb[r], wa = va[r], wb = vb[r];
+      uint4 sa = ma[r], sb = mb[r];
       if (rec >= 0) {
         const int64_t row = (static_cast<int64_t>(rec) * kDiffBlock + tl[r]) * g.E;
-        sa = ldg16(store.val_k + row + e0[r]);
-        sb = ldg16(store.val_k + row + e0[r] + g.half);
-        wa = ldg16(store.val_v + row + e0[r]);
-        wb = ldg16(store.val_v + row + e0[r] + g.half);
+        sa = ldg16(vals + row + e0[r]);
+        sb = ldg16(vals + row + e0[r] + g.half);
       }
       const int ab = a * rd.M + blk[r];
       const int pos = __ldg(rd.off + ab) + u[r];
-      uint16_t* kdst = pool_row(pool, g.E, a, layer, 0, pos, err);
-      if (!kdst) continue;
-      if (kRotate) {
+      uint16_t* dst = pool_row(pool, g.E, a, layer, un.kv, pos, err);
+      if (!dst) continue;
+      if (kRotate && un.kv == 0) {
         const int64_t toff = static_cast<int64_t>(ab) * g.half + f0[r];
         uint4 ya, yb;
         rotate_pairs<false>(sa, sb, rd.cos_t + toff, rd.sin_t + toff, ya, yb);
         sa = ya;
         sb = yb;
       }
-      st16(kdst + e0[r], sa);
-      st16(kdst + e0[r] + g.half, sb);
-      uint16_t* vdst = kdst + pool.num_pages * static_cast<int64_t>(pool.P) * g.E;
-      st16(vdst + e0[r], wa);
-      st16(vdst + e0[r] + g.half, wb);
+      st16(dst + e0[r], sa);
+      st16(dst + e0[r] + g.half, sb);
     }
   }
 }
@@ -92,13 +86,13 @@ static cudaError_t go(const Geom& g, const RoundDev& rd, const PoolDev& pool,
                       const StoreDev& store, const AgentList& agents, int layer_begin,
                       int store_layer0, int nl, int frame, uint32_t* err, cudaStream_t st) {
   const int tpl = rd.nb;
-  const int64_t tiles = static_cast<int64_t>(tpl) * nl;
-  if (tiles == 0 || agents.n == 0) return cudaSuccess;
+  const int64_t units = static_cast<int64_t>(tpl) * nl * 2 * parts_per_tile(g);
+  if (units == 0 || agents.n == 0) return cudaSuccess;
   if (frame == 0)
-    restore_kernel<kItems, true><<<static_cast<unsigned>(tiles), tile_threads(g), 0, st>>>(
+    restore_kernel<kItems, true><<<static_cast<unsigned>(units), tile_threads(g), 0, st>>>(
         g, rd, pool, store, agents, layer_begin, store_layer0, tpl, err);
   else
-    restore_kernel<kItems, false><<<static_cast<unsigned>(tiles), tile_threads(g), 0, st>>>(
+    restore_kernel<kItems, false><<<static_cast<unsigned>(units), tile_threads(g), 0, st>>>(
         g, rd, pool, store, agents, layer_begin, store_layer0, tpl, err);
   return cudaGetLastError();
 }
@@ -107,12 +101,9 @@ cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& poo
                            const StoreDev& store, const AgentList& agents, int layer_begin,
                            int store_layer0, int nl, int frame, uint32_t* err,
                            cudaStream_t st) {
-  const int items = kDiffBlock * g.vpt;
-  const int per = (items + tile_threads(g) - 1) / tile_threads(g);
-  if (per <= 1) return go<1>(g, rd, pool, store, agents, layer_begin, store_layer0, nl, frame, err, st);
-  if (per <= 2) return go<2>(g, rd, pool, store, agents, layer_begin, store_layer0, nl, frame, err, st);
-  if (per <= 4) return go<4>(g, rd, pool, store, agents, layer_begin, store_layer0, nl, frame, err, st);
-  return go<8>(g, rd, pool, store, agents, layer_begin, store_layer0, nl, frame, err, st);
+  if (tile_items(g) == 1)
+    return go<1>(g, rd, pool, store, agents, layer_begin, store_layer0, nl, frame, err, st);
+  return go<2>(g, rd, pool, store, agents, layer_begin, store_layer0, nl, frame, err, st);
 }
 
 }  // namespace td

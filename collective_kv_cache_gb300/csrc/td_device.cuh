@@ -98,6 +98,35 @@ __device__ __forceinline__ Item item_of(const Geom& g, int q) {
   return it;
 }
 
+// ---- Work units of the tile kernels: (layer, diff block, K or V, part). A part covers at
+// most kPartItems pair-vectors of the tile (two per thread at 256 threads), so E up to
+// 2048 never needs more than two items per thread.
+constexpr int kPartItems = 512;
+
+struct Unit {
+  int li;     // layer index within the launch
+  int b;      // diff block
+  int kv;     // 0 = K, 1 = V
+  int q0;     // first item of the part
+};
+
+__host__ __device__ __forceinline__ int parts_per_tile(const Geom& g) {
+  return (kDiffBlock * g.vpt + kPartItems - 1) / kPartItems;
+}
+
+__device__ __forceinline__ Unit unit_of(const Geom& g, int64_t idx, int tiles_per_layer) {
+  const int parts = parts_per_tile(g);
+  Unit u;
+  const int part = static_cast<int>(idx % parts);
+  idx /= parts;
+  u.kv = static_cast<int>(idx & 1);
+  idx >>= 1;
+  u.li = static_cast<int>(idx / tiles_per_layer);
+  u.b = static_cast<int>(idx - static_cast<int64_t>(u.li) * tiles_per_layer);
+  u.q0 = part * kPartItems;
+  return u;
+}
+
 // Row address of (agent, layer, kv, position) in the paged pool, or nullptr (and the
 // error bit) when the page is unmapped or out of range.
 __device__ __forceinline__ uint16_t* pool_row(const PoolDev& p, int E, int agent, int layer,

@@ -37,12 +37,13 @@ struct td_ctx {
 
   // scratch
   float* d_dev = nullptr;           // [max_agents * max_shared]
-  int32_t* d_rank = nullptr;        // [max_agents * max_shared]
+  uint32_t* d_selbits = nullptr;    // [max_agents * max_nb]
+  int32_t* d_firstrank = nullptr;   // [max_agents * max_nb]
   uint32_t* d_mask = nullptr;       // [max_agents * nbw_max]
   uint32_t* d_cand = nullptr;       // [max_agents * nbw_max]
   int32_t* d_wprefix = nullptr;     // [max_agents * nbw_max + max_agents]
   int64_t* d_aprefix = nullptr;     // [max_agents + 1]
-  uint8_t* d_flag = nullptr;        // [max_agents * L * max_nb]
+  uint32_t* d_flag = nullptr;       // [max_agents * L * max_nb] flags + [max_agents * L] counts
   int32_t* d_ints = nullptr;        // need_fixup, m_ok, over, spare
   int64_t* d_bound = nullptr;
   uint32_t* d_err = nullptr;
@@ -69,7 +70,8 @@ void free_ctx(td_ctx* c) {
   cudaFree(c->d_tok_block);
   cudaFree(c->d_blk_start);
   cudaFree(c->d_dev);
-  cudaFree(c->d_rank);
+  cudaFree(c->d_selbits);
+  cudaFree(c->d_firstrank);
   cudaFree(c->d_mask);
   cudaFree(c->d_cand);
   cudaFree(c->d_wprefix);
@@ -278,12 +280,14 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   chk(cudaMalloc(&c->d_tok_block, static_cast<size_t>(max_shared) * 4));
   chk(cudaMalloc(&c->d_blk_start, static_cast<size_t>(max_blocks) * 4));
   chk(cudaMalloc(&c->d_dev, NS * 4));
-  chk(cudaMalloc(&c->d_rank, NS * 4));
+  chk(cudaMalloc(&c->d_selbits, static_cast<size_t>(max_agents) * max_nb * 4));
+  chk(cudaMalloc(&c->d_firstrank, static_cast<size_t>(max_agents) * max_nb * 4));
   chk(cudaMalloc(&c->d_mask, static_cast<size_t>(max_agents) * nbw * 4));
   chk(cudaMalloc(&c->d_cand, static_cast<size_t>(max_agents) * nbw * 4));
   chk(cudaMalloc(&c->d_wprefix, (static_cast<size_t>(max_agents) * nbw + max_agents) * 4));
   chk(cudaMalloc(&c->d_aprefix, (static_cast<size_t>(max_agents) + 1) * 8));
-  chk(cudaMalloc(&c->d_flag, static_cast<size_t>(max_agents) * s.n_layers * max_nb));
+  chk(cudaMalloc(&c->d_flag, (static_cast<size_t>(max_agents) * s.n_layers * max_nb +
+                              static_cast<size_t>(max_agents) * s.n_layers) * 4));
   chk(cudaMalloc(&c->d_ints, 4 * sizeof(int32_t)));
   chk(cudaMalloc(&c->d_bound, sizeof(int64_t)));
   chk(cudaMalloc(&c->d_err, sizeof(uint32_t)));
@@ -428,12 +432,15 @@ td_status td_diff_encode(td_ctx* c, const td_round* r, const int32_t* master,
   sd.capacity = store->capacity_blocks;
   sd.nl = nl;
   EncodeScratch sc;
-  sc.rank = c->d_rank;
+  sc.selbits = c->d_selbits;
+  sc.firstrank = c->d_firstrank;
   sc.mask = c->d_mask;
   sc.cand = c->d_cand;
   sc.word_prefix = c->d_wprefix;
   sc.agent_prefix = c->d_aprefix;
   sc.flag = c->d_flag;
+  sc.row_count = reinterpret_cast<int32_t*>(
+      c->d_flag + static_cast<size_t>(c->N) * nl * ((c->S + kDiffBlock - 1) / kDiffBlock));
   sc.need_fixup = c->d_ints;
   sc.nbw = (((c->S + kDiffBlock - 1) / kDiffBlock) + 31) / 32;
   cudaError_t e = launch_encode(c->g, round_dev(c), master,

@@ -66,17 +66,21 @@ struct StoreDev {
 
 // Encode scratch (owned by the context).
 struct EncodeScratch {
-  int32_t* rank;             // [N][S] index of t in sel_i, or -1
+  uint32_t* selbits;         // [N][nb] selected tokens of agent i in diff block b (16 bits)
+  int32_t* firstrank;        // [N][nb] rank in sel_i of the block's first selected token
   uint32_t* mask;            // [N][nbw] blocks holding a selected token of agent i
   uint32_t* cand;            // [N][nbw] mask_i | mask_m for i != m, 0 for the master
-  int32_t* word_prefix;      // [N][nbw] candidates of agent i in words before w
+  int32_t* word_prefix;      // [N][nbw] candidates of agent i in words before w; then [N]
   int64_t* agent_prefix;     // [N+1] candidates per layer of agents before i
-  uint8_t* flag;             // [N][nl][nb] candidate block differs from the master's
+  uint32_t* flag;            // [N][nl][nb] candidate block differs from the master's
+  int32_t* row_count;        // [N][nl] records per row; directly after flag (one memset)
   int32_t* need_fixup;       // 1 when some candidate equalled the master's block
   int nbw;
 };
 
+// Threads per CTA of the tile kernels and items per thread (1 or 2).
 int tile_threads(const Geom& g);
+int tile_items(const Geom& g);
 
 cudaError_t launch_rerotate(const Geom& g, const RoundDev& rd, const PoolDev& pool,
                             const uint16_t* kc, const uint16_t* vc, int layer_begin, int nl,
