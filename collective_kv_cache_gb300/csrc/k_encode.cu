@@ -221,29 +221,47 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
     st16(mdst + row + h.e0[r] + a.g.half, m1[r]);
   }
 
+  // per-agent facts of this block, one chunk of agents at a time
+  __shared__ int64_t s_place[kAgentChunk];   // candidate place, -1 = not a candidate
+  __shared__ unsigned s_bits[kAgentChunk];
+  __shared__ int s_first[kAgentChunk];
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  for (int i = 0; i < N; ++i) {
-    const unsigned word = a.sc.cand[i * nbw + (b >> 5)];
-    if (!((word >> (b & 31)) & 1u)) continue;         // uniform across the CTA
-    const unsigned ibits = a.sc.selbits[static_cast<int64_t>(i) * nb + b];
-    const int ifirst = ibits ? a.sc.firstrank[static_cast<int64_t>(i) * nb + b] : 0;
-    const int64_t rec = cand_place(a, i, li, b);
-    bool d = false;
-#pragma unroll
-    for (int r = 0; r < kItems; ++r) {
-      if (h.live[r]) {
-        uint4 x0, x1;
-        agent_item<kItems>(a, i, li, kv, ibits, ifirst, h, r, x0, x1);
-        d |= neq16(x0, m0[r]) | neq16(x1, m1[r]);
-        if (!over) store_item<kItems>(a, kv, rec, h, r, x0, x1);
-      } else if (h.pad[r] && !over) {
-        store_item<kItems>(a, kv, rec, h, r, z, z);
-      }
+  for (int c0 = 0; c0 < N; c0 += kAgentChunk) {
+    const int n = min(kAgentChunk, N - c0);
+    if (c0 > 0) __syncthreads();
+    for (int x = threadIdx.x; x < n; x += blockDim.x) {
+      const int i = c0 + x;
+      const unsigned word = a.sc.cand[i * nbw + (b >> 5)];
+      const bool is_cand = (word >> (b & 31)) & 1u;
+      const unsigned ibits = is_cand ? a.sc.selbits[static_cast<int64_t>(i) * nb + b] : 0u;
+      s_place[x] = is_cand ? cand_place(a, i, li, b) : -1;
+      s_bits[x] = ibits;
+      s_first[x] = ibits ? a.sc.firstrank[static_cast<int64_t>(i) * nb + b] : 0;
     }
-    if (__any_sync(0xFFFFFFFFu, d) && lane == 0) {
-      const int64_t f = (static_cast<int64_t>(i) * a.nl + li) * nb + b;
-      if (atomicOr(a.sc.flag + f, 1u) == 0u)
-        atomicAdd(a.sc.row_count + static_cast<int64_t>(i) * a.nl + li, 1);
+    __syncthreads();
+    for (int x = 0; x < n; ++x) {
+      const int64_t rec = s_place[x];
+      if (rec < 0) continue;                       // uniform across the CTA
+      const int i = c0 + x;
+      const unsigned ibits = s_bits[x];
+      const int ifirst = s_first[x];
+      bool d = false;
+#pragma unroll
+      for (int r = 0; r < kItems; ++r) {
+        if (h.live[r]) {
+          uint4 x0, x1;
+          agent_item<kItems>(a, i, li, kv, ibits, ifirst, h, r, x0, x1);
+          d |= neq16(x0, m0[r]) | neq16(x1, m1[r]);
+          if (!over) store_item<kItems>(a, kv, rec, h, r, x0, x1);
+        } else if (h.pad[r] && !over) {
+          store_item<kItems>(a, kv, rec, h, r, z, z);
+        }
+      }
+      if (__any_sync(0xFFFFFFFFu, d) && lane == 0) {
+        const int64_t f = (static_cast<int64_t>(i) * a.nl + li) * nb + b;
+        if (atomicOr(a.sc.flag + f, 1u) == 0u)
+          atomicAdd(a.sc.row_count + static_cast<int64_t>(i) * a.nl + li, 1);
+      }
     }
   }
 }

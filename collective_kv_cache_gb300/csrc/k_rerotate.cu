@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(256, 4)
 rerotate_kernel(Geom g, RoundDev rd, PoolDev pool, const uint16_t* __restrict__ kc,
                 const uint16_t* __restrict__ vc, int layer_begin, int tiles_per_layer,
                 uint32_t* err) {
+  __shared__ int64_t s_row[kAgentChunk * kDiffBlock];  // pool row of (agent, token)
   const Unit un = unit_of(g, blockIdx.x, tiles_per_layer);
   if (un.kv == 1 && vc == nullptr) return;
   const uint16_t* src = un.kv == 0 ? kc : vc;
@@ -24,7 +25,7 @@ rerotate_kernel(Geom g, RoundDev rd, PoolDev pool, const uint16_t* __restrict__ 
   const int n_items = kDiffBlock * g.vpt;
 
   uint4 xa[kItems], xb[kItems];
-  int e0[kItems], f0[kItems], blk[kItems], u[kItems];
+  int e0[kItems], f0[kItems], tl[kItems], blk[kItems];
   bool live[kItems];
 #pragma unroll
   for (int r = 0; r < kItems; ++r) {
@@ -34,34 +35,39 @@ rerotate_kernel(Geom g, RoundDev rd, PoolDev pool, const uint16_t* __restrict__ 
     live[r] = q < n_items && t < rd.S;
     e0[r] = it.e0;
     f0[r] = it.f0;
+    tl[r] = it.tok;
     blk[r] = 0;
-    u[r] = 0;
     if (live[r]) {
       const uint16_t* row = src + (static_cast<int64_t>(un.li) * rd.S + t) * g.E;
       xa[r] = ldg16(row + it.e0);
       xb[r] = ldg16(row + it.e0 + g.half);
       blk[r] = __ldg(rd.tok_block + t);
-      u[r] = t - __ldg(rd.blk_start + blk[r]);
     }
   }
 
-  for (int i = 0; i < rd.N; ++i) {
+  for (int c0 = 0; c0 < rd.N; c0 += kAgentChunk) {
+    const int n = min(kAgentChunk, rd.N - c0);
+    if (c0 > 0) __syncthreads();  // the previous chunk's rows are no longer read
+    chunk_rows(rd, pool, layer, un.kv, t0, n, [&](int x) { return c0 + x; }, s_row, err);
+    __syncthreads();
+    for (int x = 0; x < n; ++x) {
+      const int i = c0 + x;
 #pragma unroll
-    for (int r = 0; r < kItems; ++r) {
-      if (!live[r]) continue;
-      const int ab = i * rd.M + blk[r];
-      const int pos = __ldg(rd.off + ab) + u[r];
-      uint16_t* dst = pool_row(pool, g.E, i, layer, un.kv, pos, err);
-      if (!dst) continue;
-      if (un.kv == 0) {
-        const int64_t toff = static_cast<int64_t>(ab) * g.half + f0[r];
-        uint4 ya, yb;
-        rotate_pairs<false>(xa[r], xb[r], rd.cos_t + toff, rd.sin_t + toff, ya, yb);
-        st16(dst + e0[r], ya);
-        st16(dst + e0[r] + g.half, yb);
-      } else {
-        st16(dst + e0[r], xa[r]);
-        st16(dst + e0[r] + g.half, xb[r]);
+      for (int r = 0; r < kItems; ++r) {
+        if (!live[r]) continue;
+        const int64_t row = s_row[x * kDiffBlock + tl[r]];
+        if (row < 0) continue;
+        uint16_t* dst = pool.base + row * g.E;
+        if (un.kv == 0) {
+          const int64_t toff = static_cast<int64_t>(i * rd.M + blk[r]) * g.half + f0[r];
+          uint4 ya, yb;
+          rotate_pairs<false>(xa[r], xb[r], rd.cos_t + toff, rd.sin_t + toff, ya, yb);
+          st16(dst + e0[r], ya);
+          st16(dst + e0[r] + g.half, yb);
+        } else {
+          st16(dst + e0[r], xa[r]);
+          st16(dst + e0[r] + g.half, xb[r]);
+        }
       }
     }
   }

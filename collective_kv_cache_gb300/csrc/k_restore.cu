@@ -17,6 +17,8 @@ template <int kItems, bool kRotate>
 __global__ void __launch_bounds__(256, 3)
 restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agents,
                int layer_begin, int store_layer0, int tiles_per_layer, uint32_t* err) {
+  __shared__ int64_t s_row[kAgentChunk * kDiffBlock];  // pool row of (agent, token)
+  __shared__ int s_rec[kAgentChunk];                    // record of (agent), -1 none, -2 bad
   const Unit un = unit_of(g, blockIdx.x, tiles_per_layer);
   const int t0 = un.b * kDiffBlock;
   const int layer = layer_begin + un.li;
@@ -26,7 +28,7 @@ restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agen
   const uint16_t* vals = un.kv == 0 ? store.val_k : store.val_v;
 
   uint4 ma[kItems], mb[kItems];
-  int e0[kItems], f0[kItems], tl[kItems], blk[kItems], u[kItems];
+  int e0[kItems], f0[kItems], tl[kItems], blk[kItems];
   bool live[kItems];
 #pragma unroll
   for (int r = 0; r < kItems; ++r) {
@@ -38,45 +40,71 @@ restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agen
     f0[r] = it.f0;
     tl[r] = it.tok;
     blk[r] = 0;
-    u[r] = 0;
     if (live[r]) {
       const int64_t row = (static_cast<int64_t>(sl) * rd.S + t) * g.E;
       ma[r] = ldg16(master + row + it.e0);
       mb[r] = ldg16(master + row + it.e0 + g.half);
       blk[r] = __ldg(rd.tok_block + t);
-      u[r] = t - __ldg(rd.blk_start + blk[r]);
     }
   }
 
-  for (int x = 0; x < agents.n; ++x) {
-    const int a = agents.a[x];
-    const int rec = __ldg(store.slot + (static_cast<int64_t>(a) * store.nl + sl) * rd.nb + un.b);
-    if (rec >= store.capacity) {  // a slot map that does not belong to this store
-      if (threadIdx.x == 0) atomicOr(err, err_bit(TD_ERR_INVALID_ARG));
-      continue;
+  for (int c0 = 0; c0 < agents.n; c0 += kAgentChunk) {
+    const int n = min(kAgentChunk, agents.n - c0);
+    if (c0 > 0) __syncthreads();  // the previous chunk's tables are no longer read
+    chunk_rows(rd, pool, layer, un.kv, t0, n, [&](int x) { return agents.a[c0 + x]; }, s_row,
+               err);
+    for (int x = threadIdx.x; x < n; x += blockDim.x) {
+      const int a = agents.a[c0 + x];
+      int rec = __ldg(store.slot + (static_cast<int64_t>(a) * store.nl + sl) * rd.nb + un.b);
+      if (rec >= store.capacity) {  // a slot map that does not belong to this store
+        atomicOr(err, err_bit(TD_ERR_INVALID_ARG));
+        rec = -2;
+      }
+      s_rec[x] = rec;
     }
+    __syncthreads();
+
+    // source of agent x: its record, or the Master; fetched one agent ahead
+    uint4 na[kItems], nb[kItems];
+    auto fetch = [&](int x) {
+      const int rec = s_rec[x];
 #pragma unroll
-    for (int r = 0; r < kItems; ++r) {
-      if (!live[r]) continue;
-      uint4 sa = ma[r], sb = mb[r];
-      if (rec >= 0) {
-        const int64_t row = (static_cast<int64_t>(rec) * kDiffBlock + tl[r]) * g.E;
-        sa = ldg16(vals + row + e0[r]);
-        sb = ldg16(vals + row + e0[r] + g.half);
+      for (int r = 0; r < kItems; ++r) {
+        na[r] = ma[r];
+        nb[r] = mb[r];
+        if (live[r] && rec >= 0) {
+          const int64_t row = (static_cast<int64_t>(rec) * kDiffBlock + tl[r]) * g.E;
+          na[r] = ldg16(vals + row + e0[r]);
+          nb[r] = ldg16(vals + row + e0[r] + g.half);
+        }
       }
-      const int ab = a * rd.M + blk[r];
-      const int pos = __ldg(rd.off + ab) + u[r];
-      uint16_t* dst = pool_row(pool, g.E, a, layer, un.kv, pos, err);
-      if (!dst) continue;
-      if (kRotate && un.kv == 0) {
-        const int64_t toff = static_cast<int64_t>(ab) * g.half + f0[r];
-        uint4 ya, yb;
-        rotate_pairs<false>(sa, sb, rd.cos_t + toff, rd.sin_t + toff, ya, yb);
-        sa = ya;
-        sb = yb;
+    };
+    fetch(0);
+    for (int x = 0; x < n; ++x) {
+      uint4 ca[kItems], cb[kItems];
+#pragma unroll
+      for (int r = 0; r < kItems; ++r) {
+        ca[r] = na[r];
+        cb[r] = nb[r];
       }
-      st16(dst + e0[r], sa);
-      st16(dst + e0[r] + g.half, sb);
+      const bool skip = s_rec[x] == -2;
+      if (x + 1 < n) fetch(x + 1);
+      if (skip) continue;
+      const int a = agents.a[c0 + x];
+#pragma unroll
+      for (int r = 0; r < kItems; ++r) {
+        if (!live[r]) continue;
+        const int64_t row = s_row[x * kDiffBlock + tl[r]];
+        if (row < 0) continue;
+        uint16_t* dst = pool.base + row * g.E;
+        uint4 sa = ca[r], sb = cb[r];
+        if (kRotate && un.kv == 0) {
+          const int64_t toff = static_cast<int64_t>(a * rd.M + blk[r]) * g.half + f0[r];
+          rotate_pairs<false>(ca[r], cb[r], rd.cos_t + toff, rd.sin_t + toff, sa, sb);
+        }
+        st16(dst + e0[r], sa);
+        st16(dst + e0[r] + g.half, sb);
+      }
     }
   }
 }

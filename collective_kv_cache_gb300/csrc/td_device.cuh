@@ -127,6 +127,44 @@ __device__ __forceinline__ Unit unit_of(const Geom& g, int64_t idx, int tiles_pe
   return u;
 }
 
+// Agents handled per shared-memory chunk by the tile kernels (row table 64 x 16 x 8 B).
+constexpr int kAgentChunk = 64;
+
+// Row index (in elements / E) of the token at prompt position `pos` of `agent`, layer and
+// kv in the paged pool, or -1 (and the error bit) when its page is unmapped.
+__device__ __forceinline__ int64_t pool_row_index(const PoolDev& p, int agent, int layer,
+                                                  int kv, int pos, uint32_t* err) {
+  const int lp = p.p_shift >= 0 ? (pos >> p.p_shift) : pos / p.P;
+  const int slot = pos - lp * p.P;
+  int32_t page = -1;
+  if (lp < p.max_lp) page = __ldg(p.bt + static_cast<int64_t>(agent) * p.max_lp + lp);
+  if (page < 0 || page >= p.num_pages) {
+    atomicOr(err, err_bit(TD_ERR_UNMAPPED_PAGE));
+    return -1;
+  }
+  return ((static_cast<int64_t>(layer) * 2 + kv) * p.num_pages + page) * p.P + slot;
+}
+
+// Fills s_row[x * 16 + tok] with the pool row of token t0 + tok of agent agent_of(x) for
+// the x < n agents of one chunk (-1 past the shared span or when unmapped).
+template <typename AgentOf>
+__device__ __forceinline__ void chunk_rows(const RoundDev& rd, const PoolDev& pool, int layer,
+                                           int kv, int t0, int n, AgentOf agent_of,
+                                           int64_t* s_row, uint32_t* err) {
+  for (int idx = threadIdx.x; idx < n * kDiffBlock; idx += blockDim.x) {
+    const int x = idx / kDiffBlock;
+    const int t = t0 + (idx - x * kDiffBlock);
+    int64_t row = -1;
+    if (t < rd.S) {
+      const int a = agent_of(x);
+      const int j = __ldg(rd.tok_block + t);
+      const int pos = __ldg(rd.off + a * rd.M + j) + t - __ldg(rd.blk_start + j);
+      row = pool_row_index(pool, a, layer, kv, pos, err);
+    }
+    s_row[idx] = row;
+  }
+}
+
 // Row address of (agent, layer, kv, position) in the paged pool, or nullptr (and the
 // error bit) when the page is unmapped or out of range.
 __device__ __forceinline__ uint16_t* pool_row(const PoolDev& p, int E, int agent, int layer,
