@@ -161,48 +161,28 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 def setup_round(cfg, seed, device):
+    """Round inputs resident on the device; the synthetic recompute (reused K plus seeded
+    noise) is prepared here, before any timing."""
     import torch
     from collective_kv_cache_gb300 import runner as R
-    from collective_kv_cache_gb300 import synth
+    from collective_kv_cache_gb300 import synth, workload
 
     rnd = synth.make_round(cfg, seed)
-    kc_bits, vc_bits = synth.canonical_kv(cfg, seed)
     rr = R.RoundRunner(cfg, rnd.block_len, rnd.hist_len, rnd.perm, rnd.block_table,
                        rnd.num_pages, device=device)
-    kc = R.to_device_bf16(kc_bits, device)
-    vc = R.to_device_bf16(vc_bits, device)
-    del kc_bits, vc_bits
-    # Synthetic stand-in for the model's recompute (outside the path): reused K plus noise.
+    kc, vc = workload.canonical(cfg, device, seed)
     rr.rerotate(kc, vc)
-    pos = rr.positions()
-    N, L, E, P = cfg.n_agents, cfg.n_layers, cfg.elems, cfg.page_size
-    noise = synth.check_noise(rnd, seed)
-    kf = torch.empty((N, cfg.n_shared, E), dtype=torch.bfloat16, device=device)
-    for i in range(N):
-        kf[i] = (rr.gather(i, cfg.check_layer, 0, pos[i]).float()
-                 + torch.from_numpy(noise[i]).to(device)).to(torch.bfloat16)
-    del noise
+    kf = workload.fresh_check(rr, rnd, seed)
     sel = rr.check_select(kf)
     master = rr.pick_master()
     sel_np = sel.cpu().numpy()
-    k = sel_np.shape[1]
-    nk, nv = synth.selected_noise(rnd, sel_np, seed=seed)
-    kfs = torch.empty((N, L, k, E), dtype=torch.bfloat16, device=device)
-    vfs = torch.empty((N, L, k, E), dtype=torch.bfloat16, device=device)
-    for i in range(N):
-        p = torch.from_numpy(pos[i, sel_np[i]].astype(np.int64)).to(device)
-        pages = rr.bt_t[i].long()[p // P]
-        reused = rr.pool_t[:, 0, pages, p % P].reshape(L, k, E)
-        kfs[i] = (reused.float() + torch.from_numpy(nk[i]).to(device)).to(torch.bfloat16)
-        t = torch.from_numpy(sel_np[i].astype(np.int64)).to(device)
-        vfs[i] = (vc[:, t].float() + torch.from_numpy(nv[i]).to(device)).to(torch.bfloat16)
-    del nk, nv
+    kfs, vfs = workload.fresh_selected(rr, rnd, sel_np, vc, seed)
     bound = rr.candidate_bound(master)
     rr.alloc_store(max(bound, 1))
     nnz = rr.diff_encode(kc, vc, kfs, vfs)
     torch.cuda.synchronize()
-    return dict(rr=rr, kc=kc, vc=vc, kf=kf, kfs=kfs, vfs=vfs, k=k, nnz=nnz, master=master,
-                rnd=rnd)
+    return dict(rr=rr, kc=kc, vc=vc, kf=kf, kfs=kfs, vfs=vfs, k=sel_np.shape[1], nnz=nnz,
+                master=master, rnd=rnd)
 
 
 def run_step(st, agents, events=None):

@@ -6,20 +6,23 @@
 // Only blocks that hold a selected token of the Mirror or of the Master can differ (every
 // other token of both is the canonical K/V itself), so the candidate blocks of Mirror i
 // are mask_i | mask_master. Their number per layer is known before any K/V is read, which
-// gives every candidate block a fixed place in the store:
-//   prep    per agent: a 16-bit mask of its selected tokens in each diff block, the rank
-//           of the block's first selected token, and its block bitmask
-//   cand    candidate masks, per-word and per-agent prefix counts, the bound
-//           nl * sum_i |cand_i|, master sanity
+// gives every candidate block a fixed place in the store. Three launches:
+//   prep    one CTA per agent: zeroes the agent's flags and record counts, builds a
+//           16-bit mask of its selected tokens in each diff block, the rank of the
+//           block's first selected token and its block bitmask; the CTA that finishes
+//           last (a self-resetting counter; no CTA waits) builds the candidate masks, the
+//           per-word and per-agent prefix counts, the bound nl * sum_i |cand_i|, and
+//           checks the master
 //   main    one CTA per (layer, 16-token block, K or V, part): reads its canonical data
 //           once, builds the Master's (recomputed K turned back by R(-off)) and writes it,
-//           then for each candidate Mirror builds its half-tile, writes it at its
-//           candidate place and ORs "differs" into the block's flag, one atomic per warp;
-//           the warp that sets a flag first counts the record in its row. No barriers.
-//   rows    exclusive prefix sum of the per-(agent, layer) record counts (rowptr)
-//   index   block indices and the (agent, layer, block) -> record slot map
-//   fixup   only when some candidate equalled the Master's block: rewrite the kept
-//           blocks whose record moved (recomputed from the inputs, never copied)
+//           then for each candidate Mirror builds its data, writes it at its candidate
+//           place and ORs "differs" into the block's flag, one atomic per warp; the warp
+//           that sets a flag first counts the record in its row. One CTA per tile writes
+//           the slot map and block indices of the common case (every candidate kept);
+//           the CTA that finishes last turns the record counts into rowptr.
+//   fixup   only when some candidate equalled the Master's block: compacts the slot map
+//           and indices and rewrites the kept blocks whose record moved (recomputed from
+//           the inputs, never copied); otherwise it returns at once.
 // No Mirror is built densely; in the common case the inputs are read once.
 #include "td_device.cuh"
 
@@ -40,36 +43,13 @@ struct EncArgs {
   int32_t* m_ok;        // sanitized master (-1 = invalid)
   int32_t* over;        // bound exceeds capacity
   int64_t* bound;
+  int* prep_done;       // CTAs of prep finished (self-resetting)
+  int* main_done;       // CTAs of main finished (self-resetting)
   uint32_t* err;
 };
 
-__global__ void __launch_bounds__(1024) enc_prep_kernel(EncArgs a) {
-  extern __shared__ unsigned smask[];
-  const int i = blockIdx.x;
-  const int S = a.rd.S, nb = a.rd.nb, k = a.k, nbw = a.sc.nbw;
-  uint32_t* bits = a.sc.selbits + static_cast<int64_t>(i) * nb;
-  int32_t* first = a.sc.firstrank + static_cast<int64_t>(i) * nb;
-  const int32_t* sel = a.sel + static_cast<int64_t>(i) * k;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) bits[b] = 0u;
-  for (int w = threadIdx.x; w < nbw; w += blockDim.x) smask[w] = 0u;
-  __syncthreads();
-  for (int r = threadIdx.x; r < k; r += blockDim.x) {
-    const int t = __ldg(sel + r);
-    const int prev = r > 0 ? __ldg(sel + r - 1) : -1;
-    if (t < 0 || t >= S || t <= prev) {   // rows must be ascending and in range
-      atomicOr(a.err, err_bit(TD_ERR_INVALID_ARG));
-      continue;
-    }
-    const int b = t / kDiffBlock;
-    atomicOr(&bits[b], 1u << (t - b * kDiffBlock));
-    if (prev < 0 || prev / kDiffBlock != b) first[b] = r;
-    atomicOr(&smask[b >> 5], 1u << (b & 31));
-  }
-  __syncthreads();
-  for (int w = threadIdx.x; w < nbw; w += blockDim.x) a.sc.mask[i * nbw + w] = smask[w];
-}
-
-__global__ void __launch_bounds__(1024) enc_cand_kernel(EncArgs a, const int32_t* master) {
+// Candidate masks, prefix counts, bound and master check (run by the last prep CTA).
+__device__ void build_candidates(const EncArgs& a, const int32_t* master) {
   const int N = a.rd.N, nbw = a.sc.nbw;
   __shared__ int s_m;
   if (threadIdx.x == 0) {
@@ -80,13 +60,15 @@ __global__ void __launch_bounds__(1024) enc_cand_kernel(EncArgs a, const int32_t
     }
     s_m = m;
     *a.m_ok = m;
+    *a.sc.need_fixup = 0;
+    *a.over = 0;
   }
   __syncthreads();
   const int m = s_m;
   if (m < 0) return;
   for (int x = threadIdx.x; x < N * nbw; x += blockDim.x) {
     const int i = x / nbw, w = x - (x / nbw) * nbw;
-    a.sc.cand[x] = i == m ? 0u : (a.sc.mask[x] | a.sc.mask[m * nbw + w]);
+    a.sc.cand[x] = i == m ? 0u : (__ldcg(a.sc.mask + x) | __ldcg(a.sc.mask + m * nbw + w));
   }
   __syncthreads();
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
@@ -110,8 +92,47 @@ __global__ void __launch_bounds__(1024) enc_cand_kernel(EncArgs a, const int32_t
     const int over = bound > a.store.capacity ? 1 : 0;
     *a.over = over;
     if (over) atomicOr(a.err, err_bit(TD_ERR_CAPACITY));
-    *a.sc.need_fixup = 0;
   }
+}
+
+__global__ void __launch_bounds__(1024) enc_prep_kernel(EncArgs a, const int32_t* master) {
+  extern __shared__ unsigned smask[];
+  __shared__ int s_last;
+  const int i = blockIdx.x;
+  const int S = a.rd.S, nb = a.rd.nb, k = a.k, nbw = a.sc.nbw;
+  uint32_t* bits = a.sc.selbits + static_cast<int64_t>(i) * nb;
+  int32_t* first = a.sc.firstrank + static_cast<int64_t>(i) * nb;
+  const int32_t* sel = a.sel + static_cast<int64_t>(i) * k;
+  uint32_t* flags = a.sc.flag + static_cast<int64_t>(i) * a.nl * nb;
+  for (int x = threadIdx.x; x < a.nl * nb; x += blockDim.x) flags[x] = 0u;
+  for (int x = threadIdx.x; x < a.nl; x += blockDim.x) a.sc.row_count[i * a.nl + x] = 0;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) bits[b] = 0u;
+  for (int w = threadIdx.x; w < nbw; w += blockDim.x) smask[w] = 0u;
+  __syncthreads();
+  for (int r = threadIdx.x; r < k; r += blockDim.x) {
+    const int t = __ldg(sel + r);
+    const int prev = r > 0 ? __ldg(sel + r - 1) : -1;
+    if (t < 0 || t >= S || t <= prev) {   // rows must be ascending and in range
+      atomicOr(a.err, err_bit(TD_ERR_INVALID_ARG));
+      continue;
+    }
+    const int b = t / kDiffBlock;
+    atomicOr(&bits[b], 1u << (t - b * kDiffBlock));
+    if (prev < 0 || prev / kDiffBlock != b) first[b] = r;
+    atomicOr(&smask[b >> 5], 1u << (b & 31));
+  }
+  __syncthreads();
+  for (int w = threadIdx.x; w < nbw; w += blockDim.x) a.sc.mask[i * nbw + w] = smask[w];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.prep_done, 1) == static_cast<int>(gridDim.x) - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;                        // uniform across the CTA
+  __threadfence();
+  if (threadIdx.x == 0) *a.prep_done = 0;     // ready for the next call
+  build_candidates(a, master);
 }
 
 __device__ __forceinline__ int64_t cand_place(const EncArgs& a, int i, int li, int b) {
@@ -121,6 +142,38 @@ __device__ __forceinline__ int64_t cand_place(const EncArgs& a, int i, int li, i
   const unsigned below = (b & 31) ? (word & ((1u << (b & 31)) - 1u)) : 0u;
   return ap0 * a.nl + static_cast<int64_t>(li) * (ap1 - ap0) +
          a.sc.word_prefix[i * nbw + (b >> 5)] + __popc(below);
+}
+
+// Exclusive prefix sum of the per-(agent, layer) record counts -> rowptr (one CTA).
+__device__ void rows_prefix(const EncArgs& a) {
+  __shared__ long long wsum[32];
+  const int R = a.rd.N * a.nl;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int per = (R + blockDim.x - 1) / blockDim.x;
+  const int r0 = threadIdx.x * per, r1 = min(R, r0 + per);
+  long long local = 0;
+  for (int r = r0; r < r1; ++r) local += __ldcg(a.sc.row_count + r);
+  long long incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  long long before = 0;
+  for (int w = 0; w < wid; ++w) before += wsum[w];
+  long long run = before + incl - local;
+  for (int r = r0; r < r1; ++r) {
+    a.store.rowptr[r] = run;
+    run += __ldcg(a.sc.row_count + r);
+  }
+  if (threadIdx.x == blockDim.x - 1) {
+    long long total = 0;
+    for (int w = 0; w < nw; ++w) total += wsum[w];
+    a.store.rowptr[R] = total;
+    if (!*a.over && total != *a.bound) *a.sc.need_fixup = 1;
+  }
 }
 
 // Per-thread items of one half-tile (K or V) of a (layer, block) tile.
@@ -221,6 +274,7 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
     st16(mdst + row + h.e0[r] + a.g.half, m1[r]);
   }
 
+  const bool designated = kv == 0 && un.q0 == 0;   // one CTA per tile writes slot/index
   // per-agent facts of this block, one chunk of agents at a time
   __shared__ int64_t s_place[kAgentChunk];   // candidate place, -1 = not a candidate
   __shared__ unsigned s_bits[kAgentChunk];
@@ -234,9 +288,14 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
       const unsigned word = a.sc.cand[i * nbw + (b >> 5)];
       const bool is_cand = (word >> (b & 31)) & 1u;
       const unsigned ibits = is_cand ? a.sc.selbits[static_cast<int64_t>(i) * nb + b] : 0u;
-      s_place[x] = is_cand ? cand_place(a, i, li, b) : -1;
+      const int64_t place = is_cand ? cand_place(a, i, li, b) : -1;
+      s_place[x] = place;
       s_bits[x] = ibits;
       s_first[x] = ibits ? a.sc.firstrank[static_cast<int64_t>(i) * nb + b] : 0;
+      if (designated && !over) {   // slot map and index of the common case
+        a.store.slot[(static_cast<int64_t>(i) * a.nl + li) * nb + b] = static_cast<int32_t>(place);
+        if (place >= 0) a.store.block_idx[place] = b;
+      }
     }
     __syncthreads();
     for (int x = 0; x < n; ++x) {
@@ -264,70 +323,48 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
       }
     }
   }
-}
-
-// Exclusive prefix sum of the per-(agent, layer) record counts -> rowptr.
-__global__ void __launch_bounds__(1024) enc_rows_kernel(EncArgs a) {
-  __shared__ long long wsum[32];
-  if (*a.m_ok < 0) return;
-  const int R = a.rd.N * a.nl;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int per = (R + blockDim.x - 1) / blockDim.x;
-  const int r0 = threadIdx.x * per, r1 = min(R, r0 + per);
-  long long local = 0;
-  for (int r = r0; r < r1; ++r) local += a.sc.row_count[r];
-  long long incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wsum[wid] = incl;
+  // the CTA that finishes last turns the record counts into rowptr
+  __shared__ int s_last;
   __syncthreads();
-  long long before = 0;
-  for (int w = 0; w < wid; ++w) before += wsum[w];
-  long long run = before + incl - local;
-  for (int r = r0; r < r1; ++r) {
-    a.store.rowptr[r] = run;
-    run += a.sc.row_count[r];
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.main_done, 1) == static_cast<int>(gridDim.x) - 1;
   }
-  if (threadIdx.x == blockDim.x - 1) {
-    long long total = 0;
-    for (int w = 0; w < nw; ++w) total += wsum[w];
-    a.store.rowptr[R] = total;
-    if (!*a.over && total != *a.bound) *a.sc.need_fixup = 1;
-  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) *a.main_done = 0;     // ready for the next call
+  rows_prefix(a);
 }
 
-// Block indices and the slot map; one warp per (agent, layer) row.
-__global__ void __launch_bounds__(256) enc_index_kernel(EncArgs a) {
-  if (*a.m_ok < 0 || *a.over) return;
-  const int R = a.rd.N * a.nl, nb = a.rd.nb;
-  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= R) return;
-  const uint32_t* f = a.sc.flag + w * nb;
-  int32_t* slot = a.store.slot + w * nb;
-  int64_t run = a.store.rowptr[w];
-  for (int b0 = 0; b0 < nb; b0 += 32) {
-    const int b = b0 + lane;
-    const bool on = b < nb && f[b] != 0u;
-    const unsigned bal = __ballot_sync(0xFFFFFFFFu, on);
-    const int64_t pos = run + __popc(bal & ((1u << lane) - 1u));
-    if (b < nb) slot[b] = on ? static_cast<int32_t>(pos) : -1;
-    if (on) a.store.block_idx[pos] = b;
-    run += __popc(bal);
-  }
-}
-
-// Rewrites the kept blocks whose record is not at their candidate place (only when some
-// candidate turned out equal to the Master's block). Grid-stride over (tile, K/V).
+// Only when some candidate equalled the Master's block (need_fixup): (1) compact every
+// row's slot map and block indices, warp per row; (2) rewrite each kept block whose
+// final record is not its candidate place, from the inputs. The final record of a kept
+// block is rowptr of its row plus the kept blocks before it, so (2) does not depend on
+// (1). Grid-stride; returns at once in the common case.
 template <int kItems>
 __global__ void __launch_bounds__(256) enc_fixup_kernel(EncArgs a, int tiles_per_layer) {
-  if (*a.sc.need_fixup == 0) return;
+  if (__ldcg(a.sc.need_fixup) == 0) return;
   const int m = *a.m_ok;
-  if (m < 0) return;
-  const int nb = a.rd.nb;
+  if (m < 0 || *a.over) return;
+  const int nb = a.rd.nb, R = a.rd.N * a.nl;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t w = warp0; w < R; w += nwarps) {
+    const uint32_t* f = a.sc.flag + w * nb;
+    int32_t* slot = a.store.slot + w * nb;
+    int64_t run = a.store.rowptr[w];
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int b = b0 + lane;
+      const bool on = b < nb && f[b] != 0u;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, on);
+      const int64_t pos = run + __popc(bal & ((1u << lane) - 1u));
+      if (b < nb) slot[b] = on ? static_cast<int32_t>(pos) : -1;
+      if (on) a.store.block_idx[pos] = b;
+      run += __popc(bal);
+    }
+  }
   const int64_t units = static_cast<int64_t>(tiles_per_layer) * a.nl * 2 * parts_per_tile(a.g);
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const Unit un = unit_of(a.g, u, tiles_per_layer);
@@ -336,8 +373,12 @@ __global__ void __launch_bounds__(256) enc_fixup_kernel(EncArgs a, int tiles_per
     load_half<kItems>(a, li, b * kDiffBlock, kv, un.q0, h);
     for (int i = 0; i < a.rd.N; ++i) {
       if (i == m) continue;
-      const int s = a.store.slot[(static_cast<int64_t>(i) * a.nl + li) * nb + b];
-      if (s < 0 || s == cand_place(a, i, li, b)) continue;
+      const int64_t row = static_cast<int64_t>(i) * a.nl + li;
+      const uint32_t* f = a.sc.flag + row * nb;
+      if (f[b] == 0u) continue;
+      int64_t fin = a.store.rowptr[row];
+      for (int b2 = 0; b2 < b; ++b2) fin += f[b2] != 0u;
+      if (fin == cand_place(a, i, li, b)) continue;
       const unsigned ibits = a.sc.selbits[static_cast<int64_t>(i) * nb + b];
       const int ifirst = ibits ? a.sc.firstrank[static_cast<int64_t>(i) * nb + b] : 0;
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -346,9 +387,9 @@ __global__ void __launch_bounds__(256) enc_fixup_kernel(EncArgs a, int tiles_per
         if (h.live[r]) {
           uint4 x0, x1;
           agent_item<kItems>(a, i, li, kv, ibits, ifirst, h, r, x0, x1);
-          store_item<kItems>(a, kv, s, h, r, x0, x1);
+          store_item<kItems>(a, kv, fin, h, r, x0, x1);
         } else if (h.pad[r]) {
-          store_item<kItems>(a, kv, s, h, r, z, z);
+          store_item<kItems>(a, kv, fin, h, r, z, z);
         }
       }
     }
@@ -362,13 +403,7 @@ static cudaError_t run_tiles(const EncArgs& a, int threads, cudaStream_t st) {
   enc_main_kernel<kItems><<<static_cast<unsigned>(units), threads, 0, st>>>(a, tpl);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  enc_rows_kernel<<<1, 1024, 0, st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t rows = static_cast<int64_t>(a.rd.N) * a.nl;
-  enc_index_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t fix_grid = units < 1216 ? units : 1216;
-  enc_fixup_kernel<kItems><<<static_cast<unsigned>(fix_grid), threads, 0, st>>>(a, tpl);
+  enc_fixup_kernel<kItems><<<152, 256, 0, st>>>(a, tpl);
   return cudaGetLastError();
 }
 
@@ -389,22 +424,18 @@ cudaError_t launch_encode(const Geom& g, const RoundDev& rd, const int32_t* mast
   a.nl = nl;
   a.store = store;
   a.sc = sc;
-  a.m_ok = sc.need_fixup + 1;  // the context lays these three ints out after need_fixup
+  a.m_ok = sc.need_fixup + 1;   // the context lays these ints out after need_fixup
   a.over = sc.need_fixup + 2;
+  a.prep_done = sc.need_fixup + 3;
+  a.main_done = sc.need_fixup + 4;
   a.bound = bound_dev;
   a.err = err;
   if (nl <= 0) return cudaSuccess;
-  // flags and row counts start at zero (one contiguous region)
-  const size_t flag_words = static_cast<size_t>(rd.N) * nl * rd.nb;
-  cudaError_t e = cudaMemsetAsync(sc.flag, 0, (flag_words + static_cast<size_t>(rd.N) * nl) * 4, st);
+  enc_prep_kernel<<<rd.N, 1024, sc.nbw * sizeof(unsigned), st>>>(a, master);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  enc_prep_kernel<<<rd.N, 1024, sc.nbw * sizeof(unsigned), st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  enc_cand_kernel<<<1, 1024, 0, st>>>(a, master);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int threads = tile_threads(g);
-  if (tile_items(g) == 1) return run_tiles<1>(a, threads, st);
-  return run_tiles<2>(a, threads, st);
+  if (tile_items(g) == 1) return run_tiles<1>(a, tile_threads(g), st);
+  return run_tiles<2>(a, tile_threads(g), st);
 }
 
 }  // namespace td

@@ -44,7 +44,7 @@ struct td_ctx {
   int32_t* d_wprefix = nullptr;     // [max_agents * nbw_max + max_agents]
   int64_t* d_aprefix = nullptr;     // [max_agents + 1]
   uint32_t* d_flag = nullptr;       // [max_agents * L * max_nb] flags + [max_agents * L] counts
-  int32_t* d_ints = nullptr;        // need_fixup, m_ok, over, spare
+  int32_t* d_ints = nullptr;        // need_fixup, m_ok, over, prep_done, main_done, spare
   int64_t* d_bound = nullptr;
   uint32_t* d_err = nullptr;
   // pinned host words for results
@@ -288,14 +288,14 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   chk(cudaMalloc(&c->d_aprefix, (static_cast<size_t>(max_agents) + 1) * 8));
   chk(cudaMalloc(&c->d_flag, (static_cast<size_t>(max_agents) * s.n_layers * max_nb +
                               static_cast<size_t>(max_agents) * s.n_layers) * 4));
-  chk(cudaMalloc(&c->d_ints, 4 * sizeof(int32_t)));
+  chk(cudaMalloc(&c->d_ints, 8 * sizeof(int32_t)));
   chk(cudaMalloc(&c->d_bound, sizeof(int64_t)));
   chk(cudaMalloc(&c->d_err, sizeof(uint32_t)));
   chk(cudaMallocHost(&c->h_stage, c->stage_bytes));
   chk(cudaMallocHost(&c->h_words, 4 * sizeof(int64_t)));
   chk(cudaEventCreateWithFlags(&c->stage_done, cudaEventDisableTiming));
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(uint32_t));
-  if (e == cudaSuccess) e = cudaMemset(c->d_ints, 0, 4 * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->d_ints, 0, 8 * sizeof(int32_t));
   if (e != cudaSuccess) {
     free_ctx(c);
     return TD_ERR_CUDA;
@@ -369,10 +369,9 @@ td_status td_check_select(td_ctx* c, const td_round* r, int32_t check_layer,
   *k_out = k;
   float* dev = dev_out ? dev_out : c->d_dev;
   const RoundDev rd = round_dev(c);
-  cudaError_t e = launch_deviation(c->g, rd, pd, check_layer,
-                                   static_cast<const uint16_t*>(k_fresh), dev, c->d_err, st);
-  if (e == cudaSuccess) e = launch_select(dev, rd.N, rd.S, k, sel, st);
-  return cuda_status(e);
+  return cuda_status(launch_check_select(c->g, rd, pd, check_layer,
+                                         static_cast<const uint16_t*>(k_fresh), dev, k, sel,
+                                         c->d_err, st));
 }
 
 td_status td_pick_master(td_ctx* c, const td_round* r, const int32_t* sel, int32_t k,

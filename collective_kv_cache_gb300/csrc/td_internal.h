@@ -93,6 +93,11 @@ cudaError_t launch_deviation(const Geom& g, const RoundDev& rd, const PoolDev& p
 cudaError_t launch_select(const float* dev, int N, int S, int k, int32_t* sel,
                           cudaStream_t st);
 
+// Deviations, then the per-agent top-k.
+cudaError_t launch_check_select(const Geom& g, const RoundDev& rd, const PoolDev& pool,
+                                int check_layer, const uint16_t* k_fresh, float* dev, int k,
+                                int32_t* sel, uint32_t* err, cudaStream_t st);
+
 cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int k, int64_t* cost,
                                int32_t* master, uint32_t* err, cudaStream_t st);
 

@@ -72,6 +72,67 @@ def normal_f64(key, counters: np.ndarray) -> np.ndarray:
     return (s.astype(np.int64) - _IH_MEAN).astype(np.float64) / _IH_SD
 
 
+# ---------------------------------------------------------------- the same draws in torch
+# SplitMix64 on int64 tensors: products wrap modulo 2^64 like uint64, right shifts are made
+# logical by masking, so CPU and GPU tensors give the bits numpy gives.
+_T_GAMMA = int(np.array(GAMMA).astype(np.int64))
+_T_M1 = int(np.array(_M1).astype(np.int64))
+_T_M2 = int(np.array(_M2).astype(np.int64))
+
+
+def _t_shr(x, s: int):
+    return (x >> s) & ((1 << (64 - s)) - 1)
+
+
+def _t_mix(z):
+    z = (z ^ _t_shr(z, 30)) * _T_M1
+    z = (z ^ _t_shr(z, 27)) * _T_M2
+    return z ^ _t_shr(z, 31)
+
+
+def normal_torch64(key, counters, scale: float = 1.0):
+    """normal_f64(key, counters) * scale in float64, computed by torch on the counters'
+    device (counters: an int64 tensor)."""
+    import torch
+    k = int(np.array(key, dtype=np.uint64).astype(np.int64))
+    u = _t_mix(k + (counters + 1) * _T_GAMMA)
+    m = 0xFFFF
+    s = (u & m) + (_t_shr(u, 16) & m) + (_t_shr(u, 32) & m) + _t_shr(u, 48)
+    return (s - _IH_MEAN).to(torch.float64) / _IH_SD * scale
+
+
+def normal_torch(key, counters, scale: float = 1.0):
+    """normal_torch64 rounded to float32."""
+    import torch
+    return normal_torch64(key, counters, scale).to(torch.float32)
+
+
+def canonical_torch(cfg: "RoundConfig", kv: str, layer: int, device, seed=None):
+    """One layer of canonical K or V, [S][E] bf16, on `device` (same bits as canonical_kv)."""
+    import torch
+    seed = cfg.seed if seed is None else seed
+    S, E = cfg.n_shared, cfg.elems
+    ctr = torch.arange(S * E, dtype=torch.int64, device=device)
+    x = normal_torch(stream_key(seed, "canon", kv, layer), ctr)
+    return x.to(torch.bfloat16).reshape(S, E)
+
+
+def noise_rows_torch(seed, tag, agent, layer, tokens, perturbed_rows, E):
+    """_noise_rows on torch tensors (tokens, perturbed_rows on the target device)."""
+    import torch
+    lane = torch.arange(E, dtype=torch.int64, device=tokens.device)
+    ctr = (tokens.to(torch.int64)[:, None] * E + lane[None, :]).reshape(-1)
+    out = normal_torch64(stream_key(seed, tag, "small", agent, layer), ctr,
+                         1.0e-3).reshape(len(tokens), E)
+    if bool(perturbed_rows.any()):
+        tp = tokens.to(torch.int64)[perturbed_rows]
+        ctr_big = (tp[:, None] * E + lane[None, :]).reshape(-1)
+        big = normal_torch64(stream_key(seed, tag, "big", agent, layer), ctr_big,
+                             0.5).reshape(-1, E)
+        out[perturbed_rows] += big
+    return out.to(torch.float32)
+
+
 def randint(key, counters, lo: int, hi: int) -> np.ndarray:
     """Integers uniform on [lo, hi] (inclusive)."""
     span = _U(hi - lo + 1)
