@@ -246,6 +246,58 @@ __device__ __forceinline__ void store_item(const EncArgs& a, int kv, int64_t rec
   st16(dst + h.e0[r] + a.g.half, x1);
 }
 
+// ---- per-thread asynchronous staging of recomputed rows (cp.async, 16 bytes a copy)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+constexpr int kStageDepth = 3;   // candidates in flight per thread
+
+// Stage, for candidate agent `ag`, the recomputed data of this thread's selected items:
+// slot [depth][0/1][item][thread] (each thread touches only its own 16-byte cells).
+template <int kItems>
+__device__ __forceinline__ void stage_candidate(const EncArgs& a, int ag, int li, int kv,
+                                                unsigned sbits, int first,
+                                                const HalfTile<kItems>& h, uint4* slot) {
+  const uint16_t* src = kv == 0 ? a.kf : a.vf;
+#pragma unroll
+  for (int r = 0; r < kItems; ++r) {
+    if (!h.live[r] || !((sbits >> h.tl[r]) & 1u)) continue;
+    const int rk = first + __popc(sbits & ((1u << h.tl[r]) - 1u));
+    const uint16_t* row = src + ((static_cast<int64_t>(ag) * a.nl + li) * a.k + rk) * a.g.E;
+    cp_async16(slot + (0 * kItems + r) * blockDim.x + threadIdx.x, row + h.e0[r]);
+    cp_async16(slot + (1 * kItems + r) * blockDim.x + threadIdx.x, row + h.e0[r] + a.g.half);
+  }
+  cp_async_commit();
+}
+
+// Candidate agent `ag`'s value of item r from its staged data (K turned back by R(-off)).
+template <int kItems>
+__device__ __forceinline__ void staged_item(const EncArgs& a, int ag, int kv, unsigned sbits,
+                                            const HalfTile<kItems>& h, int r,
+                                            const uint4* slot, uint4& x0, uint4& x1) {
+  x0 = h.c0[r];
+  x1 = h.c1[r];
+  if (!((sbits >> h.tl[r]) & 1u)) return;
+  const uint4 fa = slot[(0 * kItems + r) * blockDim.x + threadIdx.x];
+  const uint4 fb = slot[(1 * kItems + r) * blockDim.x + threadIdx.x];
+  if (kv == 0) {
+    const int64_t toff = static_cast<int64_t>(ag * a.rd.M + h.blk[r]) * a.g.half + h.f0[r];
+    rotate_pairs<true>(fa, fb, a.rd.cos_t + toff, a.rd.sin_t + toff, x0, x1);
+  } else {
+    x0 = fa;
+    x1 = fb;
+  }
+}
+
 template <int kItems>
 __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_per_layer) {
   const int m = *a.m_ok;
@@ -279,6 +331,10 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
   __shared__ int64_t s_place[kAgentChunk];   // candidate place, -1 = not a candidate
   __shared__ unsigned s_bits[kAgentChunk];
   __shared__ int s_first[kAgentChunk];
+  __shared__ int s_list[kAgentChunk];        // the chunk's candidates, in agent order
+  __shared__ int s_nc;
+  extern __shared__ uint4 s_stage[];         // [kStageDepth][2][kItems][blockDim]
+  const int slot_cells = 2 * kItems * blockDim.x;
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   for (int c0 = 0; c0 < N; c0 += kAgentChunk) {
     const int n = min(kAgentChunk, N - c0);
@@ -298,18 +354,46 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
       }
     }
     __syncthreads();
-    for (int x = 0; x < n; ++x) {
-      const int64_t rec = s_place[x];
-      if (rec < 0) continue;                       // uniform across the CTA
+    if (threadIdx.x == 0) {
+      int nc = 0;
+      for (int x = 0; x < n; ++x)
+        if (s_place[x] >= 0) s_list[nc++] = x;
+      s_nc = nc;
+    }
+    __syncthreads();
+    const int nc = s_nc;
+    // pipeline: candidates j+1 .. j+depth-1 are being staged while j is built and stored
+#pragma unroll
+    for (int j = 0; j < kStageDepth - 1; ++j) {
+      if (j < nc) {
+        const int x = s_list[j];
+        stage_candidate<kItems>(a, c0 + x, li, kv, s_bits[x], s_first[x], h,
+                                s_stage + j * slot_cells);
+      } else {
+        cp_async_commit();
+      }
+    }
+    for (int j = 0; j < nc; ++j) {
+      const int jn = j + kStageDepth - 1;
+      if (jn < nc) {
+        const int xn = s_list[jn];
+        stage_candidate<kItems>(a, c0 + xn, li, kv, s_bits[xn], s_first[xn], h,
+                                s_stage + (jn % kStageDepth) * slot_cells);
+      } else {
+        cp_async_commit();
+      }
+      cp_async_wait<kStageDepth - 1>();           // candidate j has landed (this thread)
+      const int x = s_list[j];
       const int i = c0 + x;
+      const int64_t rec = s_place[x];
       const unsigned ibits = s_bits[x];
-      const int ifirst = s_first[x];
+      const uint4* slot = s_stage + (j % kStageDepth) * slot_cells;
       bool d = false;
 #pragma unroll
       for (int r = 0; r < kItems; ++r) {
         if (h.live[r]) {
           uint4 x0, x1;
-          agent_item<kItems>(a, i, li, kv, ibits, ifirst, h, r, x0, x1);
+          staged_item<kItems>(a, i, kv, ibits, h, r, slot, x0, x1);
           d |= neq16(x0, m0[r]) | neq16(x1, m1[r]);
           if (!over) store_item<kItems>(a, kv, rec, h, r, x0, x1);
         } else if (h.pad[r] && !over) {
@@ -322,6 +406,7 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
           atomicAdd(a.sc.row_count + static_cast<int64_t>(i) * a.nl + li, 1);
       }
     }
+    cp_async_wait<0>();
   }
   // the CTA that finishes last turns the record counts into rowptr
   __shared__ int s_last;
@@ -400,7 +485,21 @@ template <int kItems>
 static cudaError_t run_tiles(const EncArgs& a, int threads, cudaStream_t st) {
   const int tpl = a.rd.nb;
   const int64_t units = static_cast<int64_t>(tpl) * a.nl * 2 * parts_per_tile(a.g);
-  enc_main_kernel<kItems><<<static_cast<unsigned>(units), threads, 0, st>>>(a, tpl);
+  // the staging ring: kStageDepth candidates x 2 vectors x kItems per thread (48 KiB at
+  // 256 threads and two items); beyond the default window, so opt in (once per device)
+  const size_t stage = static_cast<size_t>(kStageDepth) * 2 * kItems * threads * sizeof(uint4);
+  static int opted_in_device = -1;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (opted_in_device != cur) {
+    cudaError_t e0 = cudaFuncSetAttribute(enc_main_kernel<kItems>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(kStageDepth * 2 * kItems * 256 *
+                                                           sizeof(uint4)));
+    if (e0 != cudaSuccess) return e0;
+    opted_in_device = cur;
+  }
+  enc_main_kernel<kItems><<<static_cast<unsigned>(units), threads, stage, st>>>(a, tpl);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   enc_fixup_kernel<kItems><<<152, 256, 0, st>>>(a, tpl);
