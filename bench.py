@@ -32,7 +32,7 @@ if ROOT not in sys.path:
 
 METRIC = "restore+reuse KV GB/s (% of GB300 HBM peak); agent-rounds/sec, 7B shape"
 UNIT = "GB/s"
-LAUNCHES_PER_STEP = 11   # rerotate 1, deviation+select 2, master 1, encode 6, restore 1
+LAUNCHES_PER_STEP = 8    # rerotate 1, deviation + top-k 2, master 1, encode 3, restore 1
 CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -185,6 +185,84 @@ def setup_round(cfg, seed, device):
                 master=master, rnd=rnd)
 
 
+def workload_config(name: str):
+    """qwen7b, qwen14b, scale64, tiny, or density<pct>[_p<page>] (e.g. density40_p32)."""
+    from collective_kv_cache_gb300 import synth
+    if name in synth.CONFIGS:
+        return synth.CONFIGS[name]()
+    if name.startswith("density"):
+        body = name[len("density"):]
+        pct, _, page = body.partition("_p")
+        return synth.density(int(pct), page_size=int(page) if page else 16)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def bench_chunked(args, cfg, seed, device):
+    """The same step with encode and restore run in layer chunks (for rounds whose
+    recomputed inputs do not fit beside the pool). The synthetic recompute of each chunk
+    is built between chunks, untimed; the step time is the sum of the device spans of the
+    stages, each measured with CUDA events on the launching stream."""
+    import torch
+    from collective_kv_cache_gb300 import runner as R
+    from collective_kv_cache_gb300 import synth, workload
+    C = args.chunk_layers
+    rnd = synth.make_round(cfg, seed)
+    rr = R.RoundRunner(cfg, rnd.block_len, rnd.hist_len, rnd.perm, rnd.block_table,
+                       rnd.num_pages, device=device)
+    kc, vc = workload.canonical(cfg, device, seed)
+    rr.rerotate(kc, vc)
+    kf = workload.fresh_check(rr, rnd, seed)
+    sel = rr.check_select(kf)
+    master = rr.pick_master()
+    sel_np = sel.cpu().numpy()
+    N, L = cfg.n_agents, cfg.n_layers
+    agents = list(range(N))
+    cost = int(rr.cost_t[master].item())
+    stage_ms = {n: 0.0 for n in STAGES}
+    nnz_total = 0
+
+    def span(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(rr.stream)
+        fn()
+        b.record(rr.stream)
+        b.synchronize()
+        return a.elapsed_time(b)
+
+    for step in range(args.warmup + args.steps):
+        timed = step >= args.warmup
+        t = {"rerotate": span(lambda: rr.rerotate(kc, vc)),
+             "select": span(lambda: rr.check_select(kf)),
+             "master": span(lambda: rr.pick_master(want_host=False)),
+             "encode": 0.0, "restore": 0.0}
+        nnz_step = 0
+        for l0 in range(0, L, C):
+            l1 = min(L, l0 + C)
+            kfs, vfs = workload.fresh_selected(rr, rnd, sel_np, vc, seed, l0, l1)
+            if rr.store is None or rr.store.layer_end - rr.store.layer_begin != l1 - l0 \
+                    or rr.store_t["val_k"].shape[0] < cost * (l1 - l0):
+                rr.store = rr.store_t = None
+                torch.cuda.empty_cache()
+                rr.alloc_store(max(cost * (l1 - l0), 1), l0, l1)
+            rr.store.layer_begin, rr.store.layer_end = l0, l1
+            t["encode"] += span(lambda: rr.diff_encode(kc[l0:l1], vc[l0:l1], kfs, vfs,
+                                                       layer_begin=l0, layer_end=l1,
+                                                       want_nnz=False))
+            nnz_step += int(rr.store_t["rowptr"][-1].item())
+            t["restore"] += span(lambda: rr.fused_restore(agents))
+            del kfs, vfs
+        if timed:
+            for n in STAGES:
+                stage_ms[n] += t[n]
+            nnz_total = nnz_step
+    s_, bits = rr.get_error()
+    if s_ != 0:
+        raise RuntimeError(f"device error word {bits:#x}")
+    K = args.steps
+    stage_ms = {n: v / K for n, v in stage_ms.items()}
+    return stage_ms, sel_np.shape[1], nnz_total, master
+
+
 def run_step(st, agents, events=None):
     rr = st["rr"]
     s = rr.stream
@@ -210,6 +288,17 @@ def run_step(st, agents, events=None):
 STAGES = ("rerotate", "select", "master", "encode", "restore")
 
 
+def run_overlapped(st, agents, side, ev_check, ev_master, args):
+    """One round with the check layer's selection and the master choice on a second
+    stream, overlapped with the re-rotation of the other layers (--sequential: one
+    stream, stages in order)."""
+    if args.sequential:
+        run_step(st, agents)
+        return
+    st["rr"].round_step(st["kc"], st["vc"], st["kf"], st["kfs"], st["vfs"], agents, side,
+                        ev_check, ev_master)
+
+
 def bench_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -224,10 +313,14 @@ def bench_ours(args, rank, world, local_rank):
         _build.build()
     if world > 1:
         dist.barrier()
-    cfg = synth.CONFIGS[args.workload]()
+    cfg = workload_config(args.workload)
     if args.layers:
         cfg = cfg.replace(n_layers=args.layers, name=f"{cfg.name}_first{args.layers}layers")
     seed = rank_seed(cfg.seed, rank)
+    if args.chunk_layers is None and args.workload.startswith("density"):
+        args.chunk_layers = 8
+    if args.chunk_layers:
+        return report_chunked(args, cfg, seed, device, rank, world)
     st = setup_round(cfg, seed, device)
     rr = st["rr"]
     agents = list(range(cfg.n_agents))
@@ -245,14 +338,18 @@ def bench_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device error word {bits:#x} after warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    side = torch.cuda.Stream(device, priority=-1)   # the selection's CTAs go first
+    ev_c = [torch.cuda.Event() for _ in range(K)]
+    ev_m = [torch.cuda.Event() for _ in range(K)]
+    for _ in range(2):                      # the overlapped schedule, warmed too
+        run_overlapped(st, agents, side, torch.cuda.Event(), torch.cuda.Event(), args)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     start.record(rr.stream)
     for i in range(K):
-        run_step(st, agents, evs[i])
+        run_overlapped(st, agents, side, ev_c[i], ev_m[i], args)
     end.record(rr.stream)
     torch.cuda.synchronize()
     clk.mark("load_end")
@@ -261,8 +358,14 @@ def bench_ours(args, rank, world, local_rank):
         dist.barrier()
     ms_total = start.elapsed_time(end)
     ms_max = reduce_max(ms_total, device)
+    # per-stage attribution: the same steps once more, stages in sequence, one event each
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for i in range(K):
+        run_step(st, agents, evs[i])
+    torch.cuda.synchronize()
     stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
                 for j, name in enumerate(STAGES)}
+    seq_ms = sum(stage_ms.values())
     s, bits = rr.get_error()
     if s != 0:
         raise RuntimeError(f"device error word {bits:#x} in the timed region")
@@ -288,7 +391,7 @@ def bench_ours(args, rank, world, local_rank):
         except Exception:
             traffic = None
 
-    e2e = bench_e2e(st, agents, cfg, K, device) if not args.no_e2e else None
+    e2e = bench_e2e(st, agents, cfg, K, device, args) if not args.no_e2e else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, seed, layers=args.cpu_layers)
@@ -314,7 +417,12 @@ def bench_ours(args, rank, world, local_rank):
                          "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": traffic, "peak_kind": peak_kind},
             "e2e": e2e,
-            "gpu_launches": LAUNCHES_PER_STEP * K,
+            "gpu_launches": (LAUNCHES_PER_STEP + (0 if args.sequential else
+                             (cfg.check_layer > 0) + (cfg.check_layer + 1 < L))) * K,
+            "schedule": "sequential" if args.sequential else
+                        "check layer first; selection and master on a second stream "
+                        "overlapped with the other layers' re-rotation",
+            "stages_sequential_ms": round(seq_ms, 5),
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }
@@ -324,7 +432,46 @@ def bench_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
-def bench_e2e(st, agents, cfg, K, device):
+def report_chunked(args, cfg, seed, device, rank, world):
+    stage_ms, k, nnz, master = bench_chunked(args, cfg, seed, device)
+    N, L = cfg.n_agents, cfg.n_layers
+    ms = sum(stage_ms.values())
+    ms_max = reduce_max(ms, device)
+    by = stage_bytes(cfg, N, L, k, nnz, N)
+    total = reduce_sum(float(sum(by.values())), device)
+    value = total / (ms_max * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    dom = max(("rerotate", "restore"), key=lambda n: stage_ms[n])
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "agents": N, "layers": L,
+                       "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
+                       "shared_tokens": cfg.n_shared, "page_size": cfg.page_size,
+                       "recompute_pct": cfg.recompute_pct, "layer_chunk": args.chunk_layers,
+                       "timing": "sum of per-stage device spans; the synthetic recompute "
+                                 "between layer chunks is not timed",
+                       "parallelism": f"independent rounds x{world}"},
+            "agent_rounds_per_s": round(reduce_sum(float(N), device) / (ms_max * 1e-3), 1),
+            "hbm_frac_of_peak": round(value / peak, 4), "peak_gbs": peak,
+            "stages": {n: {"ms": round(stage_ms[n], 5), "bytes": by[n],
+                           "gbs": round(by[n] / (stage_ms[n] * 1e-3) / 1e9, 1)} for n in STAGES},
+            "diff_blocks": nnz, "selected_per_agent": k, "master": master,
+            "roofline": {"bound": "hbm", "kernel": dom,
+                         "achieved": round(by[dom] / (stage_ms[dom] * 1e-3) / 1e9, 1),
+                         "peak": peak, "unit": "GB/s",
+                         "frac": round(by[dom] / (stage_ms[dom] * 1e-3) / 1e9 / peak, 4),
+                         "traffic": None, "peak_kind": peak_kind},
+            "gpu_launches": args.steps * (4 + 4 * ((L + args.chunk_layers - 1) // args.chunk_layers)),
+            "e2e": None, "cpu_baseline": None,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def bench_e2e(st, agents, cfg, K, device, args):
     """Same step through the public calls with HOST inputs: pinned host -> device copies of
     the round's inputs and a device -> host read of its result inside the timed region."""
     import torch
@@ -339,12 +486,13 @@ def bench_e2e(st, agents, cfg, K, device):
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = sum(t.numel() * t.element_size() for t in res.values())
     s = rr.stream
+    side = torch.cuda.Stream(device, priority=-1)
 
     def one():
         with torch.cuda.stream(s):
             for n in names:
                 st[n].copy_(host[n], non_blocking=True)
-        run_step(st, agents)
+        run_overlapped(st, agents, side, torch.cuda.Event(), torch.cuda.Event(), args)
         with torch.cuda.stream(s):
             for n, t in res.items():
                 res_h[n].copy_(t, non_blocking=True)
@@ -471,9 +619,13 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="qwen7b")
+    ap.add_argument("--chunk-layers", type=int, default=None,
+                    help="run encode and restore in layer chunks (density workloads: 8)")
     ap.add_argument("--layers", type=int, default=None,
                     help="same shape with fewer layers (small profiling case)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sequential", action="store_true",
+                    help="one stream, stages in order (no overlap of the selection)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-layers", type=int, default=None)
     ap.add_argument("--ref-layers", type=int, default=4)

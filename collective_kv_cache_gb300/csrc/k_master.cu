@@ -2,8 +2,9 @@
 // agent with the smallest deviation as the dense Master; §3c A2: the deviation score is
 // chosen so that the Mirrors' diffs come out sparsest).
 //
-// One CTA. Each agent's selection becomes a bitmask over the 16-token diff blocks (shared
-// memory); cost(m) = sum over i != m of popcount(mask_i | mask_m), counted by one warp per
+// One CTA per agent turns the agent's selection into a bitmask over the 16-token diff
+// blocks; the CTA that finishes last (a self-resetting counter; no CTA waits) gathers the
+// masks and counts cost(m) = sum over i != m of popcount(mask_i | mask_m), one warp per
 // candidate m; the smallest cost wins, ties to the lower index. Integer arithmetic only,
 // so the result does not depend on the order of the additions.
 #include "td_device.cuh"
@@ -13,29 +14,50 @@ namespace td {
 __global__ void __launch_bounds__(1024)
 pick_master_kernel(const int32_t* __restrict__ sel, int N, int S, int k, int nbw,
                    int64_t* __restrict__ cost_out, int32_t* __restrict__ master,
-                   uint32_t* err) {
+                   uint32_t* gmask, int* done, uint32_t* err) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned* mask = reinterpret_cast<unsigned*>(smem_raw);                       // [N][nbw]
-  long long* cost = reinterpret_cast<long long*>(smem_raw + ((static_cast<size_t>(N) * nbw * 4 + 7) & ~size_t(7)));
-  for (int x = threadIdx.x; x < N * nbw; x += blockDim.x) mask[x] = 0u;
+  unsigned* mask = reinterpret_cast<unsigned*>(smem_raw);            // [N][nbw] (last CTA)
+  __shared__ int s_last;
+  const int i = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  for (int w = threadIdx.x; w < nbw; w += blockDim.x) mask[w] = 0u;
   __syncthreads();
-  for (int64_t x = threadIdx.x; x < static_cast<int64_t>(N) * k; x += blockDim.x) {
-    const int i = static_cast<int>(x / k);
-    const int t = __ldg(sel + x);
-    if (t < 0 || t >= S) {
-      atomicOr(err, err_bit(TD_ERR_INVALID_ARG));
-      continue;
+  // the row ascends, so lanes that hit the same block are neighbours: only the first of a
+  // run sets the bit (uniform trip count keeps the warp converged)
+  const int32_t* row = sel + static_cast<int64_t>(i) * k;
+  const int trips = (k + blockDim.x - 1) / blockDim.x;
+  for (int it = 0; it < trips; ++it) {
+    const int x = it * blockDim.x + threadIdx.x;
+    int b = -1;
+    if (x < k) {
+      const int t = __ldg(row + x);
+      if (t < 0 || t >= S) atomicOr(err, err_bit(TD_ERR_INVALID_ARG));
+      else b = t / kDiffBlock;
     }
-    const int b = t / kDiffBlock;
-    atomicOr(&mask[i * nbw + (b >> 5)], 1u << (b & 31));
+    const int prev = __shfl_up_sync(0xFFFFFFFFu, b, 1);
+    if (b >= 0 && (lane == 0 || prev != b)) atomicOr(&mask[b >> 5], 1u << (b & 31));
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int w = threadIdx.x; w < nbw; w += blockDim.x) gmask[i * nbw + w] = mask[w];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(done, 1) == N - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) *done = 0;           // ready for the next call
+  for (int x = threadIdx.x; x < N * nbw; x += blockDim.x) mask[x] = __ldcg(gmask + x);
+  long long* cost = reinterpret_cast<long long*>(
+      smem_raw + ((static_cast<size_t>(N) * nbw * 4 + 7) & ~size_t(7)));
+  __syncthreads();
+  const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int m = wid; m < N; m += nw) {
     long long c = 0;
     for (int x = lane; x < N * nbw; x += 32) {
-      const int i = x / nbw, w = x - (x / nbw) * nbw;
-      if (i != m) c += __popc(mask[i * nbw + w] | mask[m * nbw + w]);
+      const int a = x / nbw, w = x - a * nbw;
+      if (a != m) c += __popc(mask[a * nbw + w] | mask[m * nbw + w]);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
@@ -54,7 +76,8 @@ pick_master_kernel(const int32_t* __restrict__ sel, int N, int S, int k, int nbw
 }
 
 cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int k, int64_t* cost,
-                               int32_t* master, uint32_t* err, cudaStream_t st) {
+                               int32_t* master, uint32_t* gmask, int* done, uint32_t* err,
+                               cudaStream_t st) {
   const int nb = (S + kDiffBlock - 1) / kDiffBlock;
   const int nbw = (nb + 31) / 32;
   const size_t smem = ((static_cast<size_t>(N) * nbw * 4 + 7) & ~size_t(7)) + 8 * static_cast<size_t>(N);
@@ -64,7 +87,9 @@ cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int k, int64_t*
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  pick_master_kernel<<<1, 1024, smem, st>>>(sel, N, S, k, nbw, cost, master, err);
+  const int threads = k >= 512 ? 1024 : 256;
+  pick_master_kernel<<<N, threads, smem, st>>>(sel, N, S, k, nbw, cost, master, gmask, done,
+                                               err);
   return cudaGetLastError();
 }
 

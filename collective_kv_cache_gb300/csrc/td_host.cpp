@@ -41,10 +41,12 @@ struct td_ctx {
   int32_t* d_firstrank = nullptr;   // [max_agents * max_nb]
   uint32_t* d_mask = nullptr;       // [max_agents * nbw_max]
   uint32_t* d_cand = nullptr;       // [max_agents * nbw_max]
+  uint32_t* d_pm_mask = nullptr;    // [max_agents * nbw_max] masks of td_pick_master
   int32_t* d_wprefix = nullptr;     // [max_agents * nbw_max + max_agents]
   int64_t* d_aprefix = nullptr;     // [max_agents + 1]
   uint32_t* d_flag = nullptr;       // [max_agents * L * max_nb] flags + [max_agents * L] counts
-  int32_t* d_ints = nullptr;        // need_fixup, m_ok, over, prep_done, main_done, spare
+  int32_t* d_ints = nullptr;        // need_fixup, m_ok, over, prep_done, main_done,
+                                    // pick_master's counter, spare
   int64_t* d_bound = nullptr;
   uint32_t* d_err = nullptr;
   // pinned host words for results
@@ -74,6 +76,7 @@ void free_ctx(td_ctx* c) {
   cudaFree(c->d_firstrank);
   cudaFree(c->d_mask);
   cudaFree(c->d_cand);
+  cudaFree(c->d_pm_mask);
   cudaFree(c->d_wprefix);
   cudaFree(c->d_aprefix);
   cudaFree(c->d_flag);
@@ -284,6 +287,7 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   chk(cudaMalloc(&c->d_firstrank, static_cast<size_t>(max_agents) * max_nb * 4));
   chk(cudaMalloc(&c->d_mask, static_cast<size_t>(max_agents) * nbw * 4));
   chk(cudaMalloc(&c->d_cand, static_cast<size_t>(max_agents) * nbw * 4));
+  chk(cudaMalloc(&c->d_pm_mask, static_cast<size_t>(max_agents) * nbw * 4));
   chk(cudaMalloc(&c->d_wprefix, (static_cast<size_t>(max_agents) * nbw + max_agents) * 4));
   chk(cudaMalloc(&c->d_aprefix, (static_cast<size_t>(max_agents) + 1) * 8));
   chk(cudaMalloc(&c->d_flag, (static_cast<size_t>(max_agents) * s.n_layers * max_nb +
@@ -383,7 +387,8 @@ td_status td_pick_master(td_ctx* c, const td_round* r, const int32_t* sel, int32
   td_status s = prepare_round(c, r, st);
   if (s != TD_OK) return s;
   if (k > c->S) return TD_ERR_INVALID_ARG;
-  cudaError_t e = launch_pick_master(sel, c->N, c->S, k, cost_out, master_dev, c->d_err, st);
+  cudaError_t e = launch_pick_master(sel, c->N, c->S, k, cost_out, master_dev, c->d_pm_mask,
+                                     c->d_ints + 5, c->d_err, st);
   if (e != cudaSuccess) return TD_ERR_CUDA;
   if (master_host) {
     int32_t* h = reinterpret_cast<int32_t*>(c->h_words);

@@ -98,8 +98,10 @@ cudaError_t launch_check_select(const Geom& g, const RoundDev& rd, const PoolDev
                                 int check_layer, const uint16_t* k_fresh, float* dev, int k,
                                 int32_t* sel, uint32_t* err, cudaStream_t st);
 
+// gmask: [N][nbw] scratch; done: a counter that is zero between calls.
 cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int k, int64_t* cost,
-                               int32_t* master, uint32_t* err, cudaStream_t st);
+                               int32_t* master, uint32_t* gmask, int* done, uint32_t* err,
+                               cudaStream_t st);
 
 cudaError_t launch_encode(const Geom& g, const RoundDev& rd, const int32_t* master,
                           const uint16_t* kc, const uint16_t* vc, const int32_t* sel, int k,

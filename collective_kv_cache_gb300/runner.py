@@ -66,13 +66,17 @@ class RoundRunner:
 
     # ------------------------------------------------------------------ stages
     def rerotate(self, kc: torch.Tensor, vc: Optional[torch.Tensor], layer_begin=0,
-                 layer_end=None):
+                 layer_end=None, stream=None):
+        """kc, vc hold the layers [layer_begin, layer_end) (row 0 = layer_begin)."""
         layer_end = self.L if layer_end is None else layer_end
         td.td_rerotate_batched(self.ctx.handle, self.round, kc.data_ptr(),
                                vc.data_ptr() if vc is not None else None, layer_begin,
-                               layer_end, self.pool, self.s)
+                               layer_end, self.pool, self._s(stream))
 
-    def check_select(self, k_fresh: torch.Tensor, check_layer=None, pct=None):
+    def _s(self, stream) -> int:
+        return self.s if stream is None else stream.cuda_stream
+
+    def check_select(self, k_fresh: torch.Tensor, check_layer=None, pct=None, stream=None):
         check_layer = self.cfg.check_layer if check_layer is None else check_layer
         pct = self.cfg.recompute_pct if pct is None else pct
         k = (pct * self.S + 99) // 100
@@ -80,17 +84,40 @@ class RoundRunner:
             self.sel_t = torch.zeros((self.N, max(k, 0)), dtype=torch.int32, device=self.device)
         got = td.td_check_select(self.ctx.handle, self.round, check_layer, self.pool,
                                  k_fresh.data_ptr(), pct, self.sel_t.data_ptr() if k else None,
-                                 self.dev_t.data_ptr(), self.s)
+                                 self.dev_t.data_ptr(), self._s(stream))
         assert got == k
         self.k = k
         return self.sel_t
 
-    def pick_master(self, sel: Optional[torch.Tensor] = None, want_host=True):
+    def pick_master(self, sel: Optional[torch.Tensor] = None, want_host=True, stream=None):
         sel = self.sel_t if sel is None else sel
         k = sel.shape[1]
         return td.td_pick_master(self.ctx.handle, self.round, sel.data_ptr() if k else None, k,
-                                 self.cost_t.data_ptr(), self.master_t.data_ptr(), self.s,
-                                 want_host=want_host)
+                                 self.cost_t.data_ptr(), self.master_t.data_ptr(),
+                                 self._s(stream), want_host=want_host)
+
+    def round_step(self, kc, vc, kf, kfs, vfs, agents, side: torch.cuda.Stream, ev_check,
+                   ev_master):
+        """One round with the check layer's selection overlapped: the check layer is
+        re-rotated first; selection and master choice run on `side` while the other layers
+        are re-rotated on the main stream; encode and restore follow on the main stream.
+        Calls on one context may overlap like this because they touch disjoint scratch
+        and the round is already prepared."""
+        c = self.cfg.check_layer
+        main = self.stream
+        self.rerotate(kc[c:c + 1], vc[c:c + 1], c, c + 1)
+        ev_check.record(main)
+        side.wait_event(ev_check)
+        self.check_select(kf, stream=side)
+        self.pick_master(want_host=False, stream=side)
+        ev_master.record(side)
+        if c > 0:
+            self.rerotate(kc[:c], vc[:c], 0, c)
+        if c + 1 < self.L:
+            self.rerotate(kc[c + 1:], vc[c + 1:], c + 1, self.L)
+        main.wait_event(ev_master)
+        self.diff_encode(kc, vc, kfs, vfs, want_nnz=False)
+        self.fused_restore(agents, frame=0)
 
     def alloc_store(self, capacity: int, layer_begin=0, layer_end=None):
         layer_end = self.L if layer_end is None else layer_end

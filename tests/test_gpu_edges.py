@@ -220,3 +220,33 @@ def test_layer_subrange_and_agent_subset():
     rr.fused_restore([2, 0], layer_begin=2, layer_end=3)
     torch.cuda.synchronize()
     assert np.array_equal(R.bits_of(rr.pool_t), pool_o)
+
+
+def test_overlapped_round_matches_oracle():
+    """Selection and master on a second stream, overlapped with the re-rotation of the
+    other layers: the store and the restored pool are still the oracle's, bit for bit."""
+    R = _R()
+    cfg = synth.qwen7b().replace(n_layers=4, check_layer=2)
+    ch = rk.run_oracle_chain(rk.make_inputs(cfg))
+    rr = _runner(cfg, ch, fill=0x2222)
+    pool_o = oracle.new_pool(cfg, ch.rnd.num_pages, fill=0x2222)
+    assert oracle.get().fused_restore(cfg, ch.desc, ch.master, ch.store, np.arange(cfg.n_agents),
+                                      pool_o, ch.rnd.num_pages, ch.rnd.block_table) == 0
+    kc, vc = R.to_device_bf16(ch.kc, "cuda"), R.to_device_bf16(ch.vc, "cuda")
+    kf = R.to_device_bf16(ch.k_fresh, "cuda")
+    kfs = R.to_device_bf16(ch.k_fresh_sel, "cuda")
+    vfs = R.to_device_bf16(ch.v_fresh_sel, "cuda")
+    rr.alloc_store(int(ch.cost[ch.master]) * cfg.n_layers)
+    side = torch.cuda.Stream()
+    for _ in range(2):                                   # twice: the second reuses everything
+        rr.round_step(kc, vc, kf, kfs, vfs, list(range(cfg.n_agents)), side,
+                      torch.cuda.Event(), torch.cuda.Event())
+    torch.cuda.synchronize()
+    assert int(rr.master_t.item()) == ch.master
+    assert np.array_equal(rr.sel_t.cpu().numpy(), ch.sel)
+    nnz = ch.store["nnz"]
+    assert np.array_equal(rr.store_t["rowptr"].cpu().numpy(), ch.store["rowptr"])
+    assert np.array_equal(R.bits_of(rr.store_t["val_k"][:nnz]), ch.store["val_k"])
+    assert np.array_equal(R.bits_of(rr.pool_t), pool_o)
+    s, bits = rr.get_error()
+    assert s == 0 and bits == 0
