@@ -33,6 +33,10 @@ if ROOT not in sys.path:
 METRIC = "restore+reuse KV GB/s (% of GB300 HBM peak); agent-rounds/sec, 7B shape"
 UNIT = "GB/s"
 LAUNCHES_PER_STEP = 8    # rerotate 1, deviation + top-k 2, master 1, encode 3, restore 1
+# DRAM bytes (read + write) per launch of the roofline kernels at the benchmarked size, from
+# one ncu capture of these kernels as they are now (dram__bytes_read.sum +
+# dram__bytes_write.sum); set an entry to None when its kernel changes.
+MEASURED_TRAFFIC = {"qwen7b": {"restore": 2335500000, "rerotate": 1550900000}}
 CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -381,15 +385,7 @@ def bench_ours(args, rank, world, local_rank):
     # dominant single-kernel stage for the roofline
     dom = max(("rerotate", "restore"), key=lambda n: stage_ms[n])
     achieved = by[dom] / (stage_ms[dom] * 1e-3) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as f:
-                tj = json.load(f)
-            traffic = tj.get(args.workload, {}).get(dom)
-        except Exception:
-            traffic = None
+    traffic = None if args.layers else MEASURED_TRAFFIC.get(args.workload, {}).get(dom)
 
     e2e = bench_e2e(st, agents, cfg, K, device, args) if not args.no_e2e else None
     cpu = None
