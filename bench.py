@@ -164,7 +164,23 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
-def setup_round(cfg, seed, device):
+def host_store(rr, capacity: int):
+    """The round's Master-Mirror store in page-locked host memory that the GPU addresses
+    directly (the pages' Storage tier; on GB300 reached over NVLink-C2C)."""
+    import torch
+    from collective_kv_cache_gb300 import td
+    S, E, B, L, N = rr.S, rr.E, rr.B, rr.L, rr.N
+    pin = lambda shape, dt: torch.zeros(shape, dtype=dt).pin_memory()
+    t = dict(master_k=pin((L, S, E), torch.bfloat16), master_v=pin((L, S, E), torch.bfloat16),
+             rowptr=pin((N * L + 1,), torch.int64), block_idx=pin((max(capacity, 1),), torch.int32),
+             val_k=pin((capacity, B, E), torch.bfloat16), val_v=pin((capacity, B, E), torch.bfloat16),
+             slot=pin((N * L * rr.nb,), torch.int32))
+    rr.store_t = t
+    rr.store = td.make_store(t["master_k"], t["master_v"], t["rowptr"], t["block_idx"],
+                             t["val_k"], t["val_v"], t["slot"])
+
+
+def setup_round(cfg, seed, device, store_on_host=False):
     """Round inputs resident on the device; the synthetic recompute (reused K plus seeded
     noise) is prepared here, before any timing."""
     import torch
@@ -182,7 +198,10 @@ def setup_round(cfg, seed, device):
     sel_np = sel.cpu().numpy()
     kfs, vfs = workload.fresh_selected(rr, rnd, sel_np, vc, seed)
     bound = rr.candidate_bound(master)
-    rr.alloc_store(max(bound, 1))
+    if store_on_host:
+        host_store(rr, max(bound, 1))
+    else:
+        rr.alloc_store(max(bound, 1))
     nnz = rr.diff_encode(kc, vc, kfs, vfs)
     torch.cuda.synchronize()
     return dict(rr=rr, kc=kc, vc=vc, kf=kf, kfs=kfs, vfs=vfs, k=sel_np.shape[1], nnz=nnz,
@@ -325,7 +344,9 @@ def bench_ours(args, rank, world, local_rank):
         args.chunk_layers = 8
     if args.chunk_layers:
         return report_chunked(args, cfg, seed, device, rank, world)
-    st = setup_round(cfg, seed, device)
+    if args.store_on_host:
+        cfg = cfg.replace(name=cfg.name + "_store_in_host_memory")
+    st = setup_round(cfg, seed, device, store_on_host=args.store_on_host)
     rr = st["rr"]
     agents = list(range(cfg.n_agents))
     N, L = cfg.n_agents, cfg.n_layers
@@ -385,7 +406,8 @@ def bench_ours(args, rank, world, local_rank):
     # dominant single-kernel stage for the roofline
     dom = max(("rerotate", "restore"), key=lambda n: stage_ms[n])
     achieved = by[dom] / (stage_ms[dom] * 1e-3) / 1e9
-    traffic = None if args.layers else MEASURED_TRAFFIC.get(args.workload, {}).get(dom)
+    traffic = None if (args.layers or args.store_on_host) else \
+        MEASURED_TRAFFIC.get(args.workload, {}).get(dom)
 
     e2e = bench_e2e(st, agents, cfg, K, device, args) if not args.no_e2e else None
     cpu = None
@@ -409,6 +431,11 @@ def bench_ours(args, rank, world, local_rank):
             "stages": {n: {"ms": round(stage_ms[n], 5), "bytes": by[n],
                            "gbs": round(by[n] / (stage_ms[n] * 1e-3) / 1e9, 1)} for n in STAGES},
             "diff_blocks": st["nnz"], "selected_per_agent": st["k"], "master": st["master"],
+            "host_link": None if not args.store_on_host else {
+                "restore_reads_gbs": round((2 * L * cfg.n_shared * cfg.elems * 2 + st["nnz"] *
+                                            (16 * cfg.elems * 4 + 4)) / (stage_ms["restore"] * 1e-3) / 1e9, 1),
+                "encode_writes_gbs": round((2 * L * cfg.n_shared * cfg.elems * 2 + st["nnz"] *
+                                            (16 * cfg.elems * 4 + 4)) / (stage_ms["encode"] * 1e-3) / 1e9, 1)},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": traffic, "peak_kind": peak_kind},
@@ -620,6 +647,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=None,
                     help="same shape with fewer layers (small profiling case)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--store-on-host", action="store_true",
+                    help="keep the Master-Mirror store in page-locked host memory (encode "
+                         "writes it, restore reads it, over the host link)")
     ap.add_argument("--sequential", action="store_true",
                     help="one stream, stages in order (no overlap of the selection)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

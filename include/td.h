@@ -97,7 +97,10 @@ typedef struct td_paged {
  *   val_k, val_v        bf16 [capacity][16][E] the Mirror's whole block; tokens past S are 0
  *   slot                int32 [N*nl*nb]       record of (agent, layer, block), or -1
  *   capacity_blocks     records the value arrays can hold
- * The Master's rows are empty. */
+ * The Master's rows are empty. The arrays may also live in page-locked host memory that
+ * the device addresses directly (cudaHostAlloc; on GB300 reached over NVLink-C2C): this
+ * is the pages' storage tier ([R] §2a "Diff serialize ... GPU->CPU/Storage", "Fused
+ * restore"), with encode writing and restore reading it in place. */
 typedef struct td_diff_store {
   void* master_k;
   void* master_v;

@@ -250,3 +250,45 @@ def test_overlapped_round_matches_oracle():
     assert np.array_equal(R.bits_of(rr.pool_t), pool_o)
     s, bits = rr.get_error()
     assert s == 0 and bits == 0
+
+
+def test_store_in_host_memory():
+    """The store may live in page-locked host memory that the GPU addresses directly
+    (NVLink-C2C on GB300): encode writes it there and restore reads it back; both match
+    the oracle bit for bit."""
+    R = _R()
+    cfg = synth.qwen7b().replace(n_layers=3)
+    ch = rk.run_oracle_chain(rk.make_inputs(cfg))
+    orc = oracle.get()
+    pool_o = oracle.new_pool(cfg, ch.rnd.num_pages, fill=0x3333)
+    assert orc.fused_restore(cfg, ch.desc, ch.master, ch.store, np.arange(cfg.n_agents), pool_o,
+                             ch.rnd.num_pages, ch.rnd.block_table) == 0
+    rr = _runner(cfg, ch, fill=0x3333)
+    kc, vc = R.to_device_bf16(ch.kc, "cuda"), R.to_device_bf16(ch.vc, "cuda")
+    sel_t = torch.from_numpy(ch.sel).cuda()
+    m = rr.pick_master(sel_t)
+    cap = rr.candidate_bound(m)
+    from collective_kv_cache_gb300 import td
+    S, E, B, L, N = cfg.n_shared, cfg.elems, cfg.diff_block, cfg.n_layers, cfg.n_agents
+    pin = lambda shape, dt: torch.zeros(shape, dtype=dt).pin_memory()
+    host = dict(master_k=pin((L, S, E), torch.bfloat16), master_v=pin((L, S, E), torch.bfloat16),
+                rowptr=pin((N * L + 1,), torch.int64), block_idx=pin((cap,), torch.int32),
+                val_k=pin((cap, B, E), torch.bfloat16), val_v=pin((cap, B, E), torch.bfloat16),
+                slot=pin((N * L * rr.nb,), torch.int32))
+    rr.store_t = host
+    rr.store = td.make_store(host["master_k"], host["master_v"], host["rowptr"],
+                             host["block_idx"], host["val_k"], host["val_v"], host["slot"])
+    nnz = rr.diff_encode(kc, vc, R.to_device_bf16(ch.k_fresh_sel, "cuda"),
+                         R.to_device_bf16(ch.v_fresh_sel, "cuda"), sel=sel_t)
+    torch.cuda.synchronize()
+    assert nnz == ch.store["nnz"]
+    assert np.array_equal(host["rowptr"].numpy(), ch.store["rowptr"])
+    assert np.array_equal(host["val_k"][:nnz].view(torch.int16).numpy().view(np.uint16),
+                          ch.store["val_k"])
+    assert np.array_equal(host["master_v"].view(torch.int16).numpy().view(np.uint16),
+                          ch.store["master_v"])
+    rr.fused_restore(list(range(N)))
+    torch.cuda.synchronize()
+    assert np.array_equal(R.bits_of(rr.pool_t), pool_o)
+    s, bits = rr.get_error()
+    assert s == 0 and bits == 0
