@@ -9,6 +9,7 @@ Parity status of each function (what pins it, beyond itself, lives in the tests)
   offsets, rope table, rotate, rerotate     pinned (closed forms, invariants, brute force)
   token deviation, top-k, check-select      pinned (exact sums, brute-force sort)
   pick_master                               pinned (exhaustive set unions)
+  pick_master_min_dev, select_group         pinned (exact sums, brute-force sort)
   diff_encode, fused_restore                pinned (bitwise round trip, closed forms)
   compression ratios                        pinned (closed form; the pages' own table)
 """
@@ -84,6 +85,10 @@ class Oracle:
         L.orc_token_dev.argtypes = [C.c_void_p, C.c_void_p, C.c_int]
         L.orc_topk.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p]
         L.orc_pick_master.argtypes = [C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int, C.c_void_p]
+        L.orc_pick_master_min_dev.argtypes = [C.c_int, C.c_int, C.c_void_p, C.c_int,
+                                              C.c_void_p, C.c_void_p]
+        L.orc_select_group.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                       C.c_void_p]
         L.orc_round_ratio.restype = C.c_double
         L.orc_round_ratio.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int64]
         L.orc_mirror_ratio.restype = C.c_double
@@ -197,6 +202,25 @@ class Oracle:
         cost = np.zeros(N, dtype=np.int64)
         m = self.lib.orc_pick_master(N, n_shared, diff_block, sel.ctypes.data, k, cost.ctypes.data)
         return int(m), cost
+
+    def pick_master_min_dev(self, sel: np.ndarray, dev: np.ndarray):
+        sel = np.ascontiguousarray(sel, dtype=np.int32)
+        dev = np.ascontiguousarray(dev, dtype=np.float32)
+        N, k = sel.shape
+        score = np.zeros(N, dtype=np.float64)
+        m = self.lib.orc_pick_master_min_dev(N, dev.shape[1], sel.ctypes.data, k, dev.ctypes.data,
+                                             score.ctypes.data)
+        return int(m), score
+
+    def select_group(self, dev: np.ndarray, k: int):
+        dev = np.ascontiguousarray(dev, dtype=np.float32)
+        N, S = dev.shape
+        row = np.zeros(max(k, 1), dtype=np.int32)
+        g = np.zeros(S, dtype=np.float32)
+        st = self.lib.orc_select_group(dev.ctypes.data, N, S, k, row.ctypes.data, g.ctypes.data)
+        if st != ORC_OK:
+            raise FloatingPointError(f"orc_select_group status {st}")
+        return row[:k].copy(), g
 
     def diff_encode(self, cfg, rnd_desc, master, k_canon, v_canon, sel, k_fresh_sel,
                     v_fresh_sel, layer_begin=0, layer_end=None, capacity=None):

@@ -300,6 +300,51 @@ int orc_pick_master(int n_agents, int n_shared, int diff_block, const int32_t* s
   return best;
 }
 
+/* Variant of the Master rule read literally: "the agent with the smallest deviation"
+ * ([R] Summary, Method (3)) taken as the total key deviation of the agent's important
+ * positions. READING of the summation: float64; addend r goes to accumulator r mod 32,
+ * each accumulator adds its addends in ascending r, then the 32 accumulators are added
+ * pairwise (l + 16, l + 8, ..., l + 1). Smallest score wins, ties to the lower index. */
+int orc_pick_master_min_dev(int n_agents, int n_shared, const int32_t* sel, int k,
+                            const float* dev, double* score) {
+  int best = -1;
+  double best_score = 0.0;
+  for (int i = 0; i < n_agents; ++i) {
+    double acc[32];
+    for (int l = 0; l < 32; ++l) acc[l] = 0.0;
+    for (int r = 0; r < k; ++r) {
+      int t = sel[(int64_t)i * k + r];
+      if (t < 0 || t >= n_shared) return -ORC_ERR_ARG;
+      acc[r % 32] = acc[r % 32] + (double)dev[(int64_t)i * n_shared + t];
+    }
+    for (int w = 16; w >= 1; w /= 2)
+      for (int l = 0; l < w; ++l) acc[l] = acc[l] + acc[l + w];
+    if (isnan(acc[0]) || isinf(acc[0])) return -ORC_ERR_NONFINITE;
+    if (score) score[i] = acc[0];
+    if (best < 0 || acc[0] < best_score) { best = i; best_score = acc[0]; }
+  }
+  return best;
+}
+
+/* Variant of the important-position set: one set for the whole group ([R] Summary,
+ * Method (2): one key-difference analysis for the batch of N requests). READING: the
+ * group deviation of token t is the float32 sum of the agents' deviations in agent order
+ * 0..N-1; the top-k of it (ties to the lower token, ascending output) is every agent's
+ * set. */
+int orc_select_group(const float* dev, int n_agents, int n_shared, int k, int32_t* sel_row,
+                     float* group_dev) {
+  float* g = malloc(sizeof(float) * (n_shared > 0 ? n_shared : 1));
+  for (int t = 0; t < n_shared; ++t) {
+    float s = 0.0f;
+    for (int i = 0; i < n_agents; ++i) s = s + dev[(int64_t)i * n_shared + t];
+    g[t] = s;
+    if (group_dev) group_dev[t] = s;
+  }
+  int st = orc_topk(g, n_shared, k, sel_row);
+  free(g);
+  return st;
+}
+
 /* ------------------------------------------------------------------ stage 3b */
 /* Agent i's cache in the canonical frame at layer l (dense, one layer): the recomputed
  * K/V at its selected tokens, K turned back by R(-off), and the reused canonical K/V

@@ -97,6 +97,17 @@ int orc_topk(const float* dev, int n, int k, int32_t* out);
 int orc_pick_master(int n_agents, int n_shared, int diff_block, const int32_t* sel, int k,
                     int64_t* cost);
 
+/* Stage 3a, variant: the agent whose selected tokens deviate least in total. score[i] =
+ * sum over the k selected tokens of dev_i, in float64, in the fixed order of the variant
+ * (see the source). Returns the master (or <0 on bad input / non-finite scores). */
+int orc_pick_master_min_dev(int n_agents, int n_shared, const int32_t* sel, int k,
+                            const float* dev, double* score);
+
+/* Stage 2, variant: one important set for the whole group: the top-k tokens of the
+ * group deviation g(t) = sum over agents of dev_i(t) (float32, agents in order). */
+int orc_select_group(const float* dev, int n_agents, int n_shared, int k, int32_t* sel_row,
+                     float* group_dev);
+
 /* Stage 3b: Master-Mirror encoding of layers [layer_begin, layer_end). */
 int orc_diff_encode(const orc_shape* sh, const orc_round* rd, int master,
                     const uint16_t* k_canon, const uint16_t* v_canon,

@@ -44,6 +44,11 @@ MUTANTS = {
     "master_ties_to_higher": ("if (best < 0 || c < best_cost)", "if (best < 0 || c <= best_cost)"),
     "master_counts_intersection": ("c += (mask[(int64_t)i * nb + b] | mask[(int64_t)m * nb + b]) ? 1 : 0;",
                                    "c += (mask[(int64_t)i * nb + b] & mask[(int64_t)m * nb + b]) ? 1 : 0;"),
+    "min_dev_argmax": ("if (best < 0 || acc[0] < best_score)", "if (best < 0 || acc[0] > best_score)"),
+    "min_dev_drops_last": ("for (int r = 0; r < k; ++r) {\n      int t = sel[(int64_t)i * k + r];\n      if (t < 0 || t >= n_shared) return -ORC_ERR_ARG;",
+                           "for (int r = 0; r < k - 1; ++r) {\n      int t = sel[(int64_t)i * k + r];\n      if (t < 0 || t >= n_shared) return -ORC_ERR_ARG;"),
+    "group_first_agent_only": ("for (int i = 0; i < n_agents; ++i) s = s + dev[(int64_t)i * n_shared + t];",
+                               "for (int i = 0; i < 1; ++i) s = s + dev[(int64_t)i * n_shared + t];"),
     # encode / restore
     "encode_compares_k_only": ("memcmp(xik + (int64_t)t0 * E, xmk + (int64_t)t0 * E, n) != 0 ||\n                        memcmp(xiv + (int64_t)t0 * E, xmv + (int64_t)t0 * E, n) != 0;",
                                "memcmp(xik + (int64_t)t0 * E, xmk + (int64_t)t0 * E, n) != 0;"),

@@ -286,6 +286,52 @@ def pin_master(orc):
     assert m == 0 and cost.tolist() == [4, 4, 4]
 
 
+def pin_master_min_dev(orc):
+    """Variant master rule: the total deviation of each agent's selected tokens."""
+    rng = np.random.default_rng(31)
+    for trial in range(30):
+        N, S = int(rng.integers(1, 7)), int(rng.integers(1, 300))
+        k = int(rng.integers(0, min(S, 80) + 1))
+        sel = np.stack([np.sort(rng.choice(S, k, replace=False)) for _ in range(N)]).astype(np.int32)
+        sel = sel.reshape(N, k)
+        dev = (rng.random((N, S)) * 100).astype(np.float32)
+        m, score = orc.pick_master_min_dev(sel, dev)
+        exact = [math.fsum(float(dev[i, t]) for t in sel[i]) for i in range(N)]
+        for i in range(N):
+            assert abs(score[i] - exact[i]) <= 1e-12 * max(1.0, abs(exact[i])), (trial, i)
+        order = sorted(range(N), key=lambda i: (exact[i], i))
+        if N > 1 and exact[order[1]] - exact[order[0]] > 1e-6 * max(1.0, abs(exact[order[0]])):
+            assert m == order[0], (trial, m, order[0])
+    # integer deviations: exact sums, ties to the lower index
+    dev = np.array([[1, 2, 3, 4], [4, 3, 2, 1], [0, 0, 9, 9]], np.float32)
+    sel = np.array([[0, 1], [2, 3], [0, 1]], np.int32)
+    m, score = orc.pick_master_min_dev(sel, dev)
+    assert score.tolist() == [3.0, 3.0, 0.0] and m == 2
+    sel = np.array([[0, 1], [2, 3], [2, 3]], np.int32)
+    m, score = orc.pick_master_min_dev(sel, dev)
+    assert score.tolist() == [3.0, 3.0, 18.0] and m == 0
+    dev[1, 2] = np.nan
+    m, _ = orc.pick_master_min_dev(sel, dev)
+    assert m < 0
+
+
+def pin_select_group(orc):
+    """Variant important set: top-k of the deviation summed over agents (integer-valued
+    deviations make every float sum exact)."""
+    rng = np.random.default_rng(33)
+    for trial in range(25):
+        N, S = int(rng.integers(1, 6)), int(rng.integers(1, 400))
+        k = int(rng.integers(0, S + 1))
+        dev = rng.integers(0, 6, (N, S)).astype(np.float32)       # many ties
+        row, g = orc.select_group(dev, k)
+        gsum = dev.astype(np.int64).sum(axis=0)
+        assert (g == gsum).all()
+        want = sorted(sorted(range(S), key=lambda t: (-int(gsum[t]), t))[:k])
+        assert row.tolist() == want, (trial, N, S, k)
+    dev = (rng.random((1, 50)) * 7).astype(np.float32)             # one agent: plain top-k
+    assert orc.select_group(dev, 9)[0].tolist() == orc.topk(dev[0], 9).tolist()
+
+
 # --------------------------------------------------------------------------- stage 3b / 4
 def _canonical_agent_cache(orc, ch, i, l):
     """Agent i's cache at layer l in the canonical frame, built from the definition."""
@@ -417,7 +463,8 @@ def pin_compression(orc):
 
 PINS = [pin_bf16, pin_offsets, pin_rope_table, pin_rotation_units, pin_rotation_bound,
         pin_rotation_group, pin_rerotate_absolute, pin_deviation, pin_topk,
-        pin_select_recovers_perturbed, pin_k_rounding, pin_master, pin_roundtrip,
+        pin_select_recovers_perturbed, pin_k_rounding, pin_master, pin_master_min_dev,
+        pin_select_group, pin_roundtrip,
         pin_v_only_difference, pin_identical_agents, pin_empty_selection_and_capacity,
         pin_compression]
 
