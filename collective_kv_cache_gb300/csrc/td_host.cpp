@@ -37,6 +37,8 @@ struct td_ctx {
 
   // scratch
   float* d_dev = nullptr;           // [max_agents * max_shared]
+  float* d_gdev = nullptr;          // [max_shared] group deviation (variant)
+  double* d_score = nullptr;        // [max_agents] deviation totals (variant)
   uint32_t* d_selbits = nullptr;    // [max_agents * max_nb]
   int32_t* d_firstrank = nullptr;   // [max_agents * max_nb]
   uint32_t* d_mask = nullptr;       // [max_agents * nbw_max]
@@ -72,6 +74,8 @@ void free_ctx(td_ctx* c) {
   cudaFree(c->d_tok_block);
   cudaFree(c->d_blk_start);
   cudaFree(c->d_dev);
+  cudaFree(c->d_gdev);
+  cudaFree(c->d_score);
   cudaFree(c->d_selbits);
   cudaFree(c->d_firstrank);
   cudaFree(c->d_mask);
@@ -283,6 +287,8 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   chk(cudaMalloc(&c->d_tok_block, static_cast<size_t>(max_shared) * 4));
   chk(cudaMalloc(&c->d_blk_start, static_cast<size_t>(max_blocks) * 4));
   chk(cudaMalloc(&c->d_dev, NS * 4));
+  chk(cudaMalloc(&c->d_gdev, static_cast<size_t>(max_shared) * 4));
+  chk(cudaMalloc(&c->d_score, static_cast<size_t>(max_agents) * 8));
   chk(cudaMalloc(&c->d_selbits, static_cast<size_t>(max_agents) * max_nb * 4));
   chk(cudaMalloc(&c->d_firstrank, static_cast<size_t>(max_agents) * max_nb * 4));
   chk(cudaMalloc(&c->d_mask, static_cast<size_t>(max_agents) * nbw * 4));
@@ -394,6 +400,53 @@ td_status td_pick_master(td_ctx* c, const td_round* r, const int32_t* sel, int32
     int32_t* h = reinterpret_cast<int32_t*>(c->h_words);
     if ((e = cudaMemcpyAsync(h, master_dev, 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
         (e = cudaStreamSynchronize(st)) != cudaSuccess)
+      return TD_ERR_CUDA;
+    *master_host = *h;
+  }
+  return TD_OK;
+}
+
+td_status td_check_select_group(td_ctx* c, const td_round* r, int32_t check_layer,
+                                const td_paged* pool, const void* k_fresh,
+                                int32_t recompute_pct, int32_t* sel, float* dev_out,
+                                float* group_dev_out, int32_t* k_out, void* stream) {
+  if (!c || !same_device(c) || !k_fresh || !aligned16(k_fresh) || !k_out)
+    return TD_ERR_INVALID_ARG;
+  if (check_layer < 0 || check_layer >= c->shape.n_layers || recompute_pct < 0 ||
+      recompute_pct > 100)
+    return TD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  td_status s = prepare_round(c, r, st);
+  if (s != TD_OK) return s;
+  PoolDev pd;
+  if ((s = pool_dev(c, r, pool, &pd)) != TD_OK) return s;
+  const int k = static_cast<int>((static_cast<int64_t>(recompute_pct) * c->S + 99) / 100);
+  if (k > 0 && !sel) return TD_ERR_INVALID_ARG;
+  *k_out = k;
+  return cuda_status(launch_check_select_group(
+      c->g, round_dev(c), pd, check_layer, static_cast<const uint16_t*>(k_fresh),
+      dev_out ? dev_out : c->d_dev, group_dev_out ? group_dev_out : c->d_gdev, k, sel,
+      c->d_err, st));
+}
+
+td_status td_pick_master_min_deviation(td_ctx* c, const td_round* r, const int32_t* sel,
+                                       int32_t k, const float* dev, double* score_out,
+                                       int32_t* master_dev, int32_t* master_host,
+                                       void* stream) {
+  if (!c || !same_device(c) || !master_dev || !dev || k < 0 || (k > 0 && !sel))
+    return TD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  td_status s = prepare_round(c, r, st);
+  if (s != TD_OK) return s;
+  if (k > c->S) return TD_ERR_INVALID_ARG;
+  cudaError_t e = launch_min_dev_master(sel, dev, c->N, c->S, k,
+                                        score_out ? score_out : c->d_score, master_dev,
+                                        c->d_err, st);
+  if (e != cudaSuccess) return TD_ERR_CUDA;
+  if (master_host) {
+    int32_t* h = reinterpret_cast<int32_t*>(c->h_words);
+    if (cudaMemcpyAsync(h, master_dev, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
       return TD_ERR_CUDA;
     *master_host = *h;
   }

@@ -103,6 +103,15 @@ cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int k, int64_t*
                                int32_t* master, uint32_t* gmask, int* done, uint32_t* err,
                                cudaStream_t st);
 
+// Variant readings (k_variants.cu).
+cudaError_t launch_min_dev_master(const int32_t* sel, const float* dev, int N, int S, int k,
+                                  double* score, int32_t* master, uint32_t* err,
+                                  cudaStream_t st);
+cudaError_t launch_check_select_group(const Geom& g, const RoundDev& rd, const PoolDev& pool,
+                                      int check_layer, const uint16_t* k_fresh, float* dev,
+                                      float* gdev, int k, int32_t* sel, uint32_t* err,
+                                      cudaStream_t st);
+
 cudaError_t launch_encode(const Geom& g, const RoundDev& rd, const int32_t* master,
                           const uint16_t* kc, const uint16_t* vc, const int32_t* sel, int k,
                           const uint16_t* kf, const uint16_t* vf, int nl,

@@ -78,6 +78,9 @@ def _load() -> C.CDLL:
         "td_get_error": [VP, VP, P(C.c_uint32)],
         "td_check_select_noalloc": [P(td_shape), P(td_round), I32, P(td_paged), VP, I32, VP,
                                     P(I32), P(C.c_uint32), VP],
+        "td_check_select_group": [VP, P(td_round), I32, P(td_paged), VP, I32, VP, VP, VP,
+                                  P(I32), VP],
+        "td_pick_master_min_deviation": [VP, P(td_round), VP, I32, VP, VP, VP, P(I32), VP],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -91,7 +94,8 @@ def _load() -> C.CDLL:
 _lib = _load()
 EXPORTS = ("td_ctx_create", "td_ctx_destroy", "td_status_string", "td_round_offsets",
            "td_rerotate_batched", "td_check_select", "td_pick_master", "td_diff_encode",
-           "td_fused_restore", "td_get_error", "td_check_select_noalloc")
+           "td_fused_restore", "td_get_error", "td_check_select_noalloc",
+           "td_check_select_group", "td_pick_master_min_deviation")
 
 
 def lib_path() -> str:
@@ -173,6 +177,30 @@ def td_fused_restore(ctx, rnd, store: td_diff_store, agents: Sequence[int], laye
     s = _lib.td_fused_restore(ctx, C.byref(rnd), C.byref(store), ag.ctypes.data, len(ag),
                               layer_begin, layer_end, frame, C.byref(pool), stream)
     return _check(s, "td_fused_restore") if check else s
+
+
+def td_check_select_group(ctx, rnd, check_layer, pool, k_fresh, recompute_pct, sel,
+                          dev_out=None, group_dev_out=None, stream=0, check=True):
+    k = C.c_int32(0)
+    s = _lib.td_check_select_group(ctx, C.byref(rnd), check_layer, C.byref(pool), k_fresh,
+                                   recompute_pct, sel, dev_out, group_dev_out, C.byref(k),
+                                   stream)
+    if check:
+        _check(s, "td_check_select_group")
+        return k.value
+    return s, k.value
+
+
+def td_pick_master_min_deviation(ctx, rnd, sel, k, dev, score_out, master_dev, stream=0,
+                                 want_host=True, check=True):
+    m = C.c_int32(-1)
+    s = _lib.td_pick_master_min_deviation(ctx, C.byref(rnd), sel, k, dev, score_out,
+                                          master_dev, C.byref(m) if want_host else None,
+                                          stream)
+    if check:
+        _check(s, "td_pick_master_min_deviation")
+        return m.value
+    return s, m.value
 
 
 def td_check_select_noalloc(shape: td_shape, rnd: td_round, check_layer, pool, k_fresh,

@@ -174,6 +174,31 @@ td_status td_pick_master(td_ctx* ctx, const td_round* round, const int32_t* sel,
                          int64_t* cost_out, int32_t* master_dev, int32_t* master_host,
                          void* stream);
 
+/* Stage 2, variant reading - one important set for the whole group. [R] Summary Method
+ * (2) speaks of one key-difference analysis for the batched requests; this variant takes
+ * it group-wide: the group deviation of token t is the float32 sum, in agent order, of
+ * the agents' deviations (defined as for td_check_select), and its top k tokens (ties to
+ * the lower token, ascending) become EVERY agent's selection: every row of sel is equal.
+ *   group_dev_out  DEVICE float [S], or NULL
+ * Other arguments as for td_check_select. */
+td_status td_check_select_group(td_ctx* ctx, const td_round* round, int32_t check_layer,
+                                const td_paged* pool, const void* k_fresh,
+                                int32_t recompute_pct, int32_t* sel, float* dev_out,
+                                float* group_dev_out, int32_t* k_out, void* stream);
+
+/* Stage 3a, variant reading - the Master is "the agent with the smallest deviation"
+ * ([R] Summary Method (3)) taken literally: score(i) = sum over i's k selected tokens of
+ * dev_i(t), in float64, addend r to accumulator r mod 32 (ascending r), then the 32
+ * accumulators added pairwise (l + 16, ..., l + 1); master = argmin, ties to the lower
+ * index. A non-finite score sets TD_ERR_NONFINITE in the error word.
+ *   dev        DEVICE float [N][S]  deviations as td_check_select writes them
+ *   score_out  DEVICE double [N], or NULL
+ * Other arguments as for td_pick_master. */
+td_status td_pick_master_min_deviation(td_ctx* ctx, const td_round* round, const int32_t* sel,
+                                       int32_t k, const float* dev, double* score_out,
+                                       int32_t* master_dev, int32_t* master_host,
+                                       void* stream);
+
 /* Stage 3b - Master-Mirror block-sparse encoding ([R] Summary Method (3): Master keeps a
  * full cache, every other agent records only the indices and values of its differing
  * blocks; Figure 8; §2a "Diff serialize: Mirror dense -> (indices, K/V)"). Agent i's
