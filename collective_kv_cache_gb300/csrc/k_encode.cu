@@ -341,24 +341,37 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
     if (c0 > 0) __syncthreads();
     for (int x = threadIdx.x; x < n; x += blockDim.x) {
       const int i = c0 + x;
+      // all facts loaded at once (one round trip); unused ones are simply ignored
       const unsigned word = a.sc.cand[i * nbw + (b >> 5)];
+      const unsigned sb = a.sc.selbits[static_cast<int64_t>(i) * nb + b];
+      const int fr = a.sc.firstrank[static_cast<int64_t>(i) * nb + b];
+      const int64_t ap0 = a.sc.agent_prefix[i], ap1 = a.sc.agent_prefix[i + 1];
+      const int wp = a.sc.word_prefix[i * nbw + (b >> 5)];
       const bool is_cand = (word >> (b & 31)) & 1u;
-      const unsigned ibits = is_cand ? a.sc.selbits[static_cast<int64_t>(i) * nb + b] : 0u;
-      const int64_t place = is_cand ? cand_place(a, i, li, b) : -1;
+      const unsigned below = (b & 31) ? (word & ((1u << (b & 31)) - 1u)) : 0u;
+      const int64_t place = is_cand ? ap0 * a.nl + static_cast<int64_t>(li) * (ap1 - ap0) + wp +
+                                          __popc(below)
+                                    : -1;
+      const unsigned ibits = is_cand ? sb : 0u;
       s_place[x] = place;
       s_bits[x] = ibits;
-      s_first[x] = ibits ? a.sc.firstrank[static_cast<int64_t>(i) * nb + b] : 0;
+      s_first[x] = ibits ? fr : 0;
       if (designated && !over) {   // slot map and index of the common case
         a.store.slot[(static_cast<int64_t>(i) * a.nl + li) * nb + b] = static_cast<int32_t>(place);
         if (place >= 0) a.store.block_idx[place] = b;
       }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {                    // compact the candidates, in agent order
       int nc = 0;
-      for (int x = 0; x < n; ++x)
-        if (s_place[x] >= 0) s_list[nc++] = x;
-      s_nc = nc;
+      for (int x0 = 0; x0 < n; x0 += 32) {
+        const int x = x0 + threadIdx.x;
+        const bool c = x < n && s_place[x] >= 0;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, c);
+        if (c) s_list[nc + __popc(bal & ((1u << threadIdx.x) - 1u))] = x;
+        nc += __popc(bal);
+      }
+      if (threadIdx.x == 0) s_nc = nc;
     }
     __syncthreads();
     const int nc = s_nc;
