@@ -51,6 +51,13 @@ class td_diff_store(C.Structure):
                 ("layer_begin", C.c_int32), ("layer_end", C.c_int32)]
 
 
+class td_prompt(C.Structure):
+    _fields_ = [("tokens", C.c_void_p), ("n_tokens", C.c_int64), ("pages", C.c_void_p)]
+
+
+TD_ROUND_OK, TD_ROUND_NO_BLOCKS, TD_ROUND_REPEATED_BLOCK, TD_ROUND_NOT_CACHED = 0, 1, 2, 3
+
+
 class TDError(RuntimeError):
     def __init__(self, status: int, where: str):
         super().__init__(f"{where}: {status_string(status)} (status {status})")
@@ -81,11 +88,16 @@ def _load() -> C.CDLL:
         "td_check_select_group": [VP, P(td_round), I32, P(td_paged), VP, I32, VP, VP, VP,
                                   P(I32), VP],
         "td_pick_master_min_deviation": [VP, P(td_round), VP, I32, VP, VP, VP, P(I32), VP],
+        "td_form_rounds": [P(td_prompt), I32, I32, I32, VP, I32, VP, VP, P(I32)],
+        "td_group_round": [P(td_prompt), I32, I32, VP, I32, I32, I32, VP, P(I32), VP, P(I32),
+                           VP, VP],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
         f.argtypes = args
         f.restype = C.c_int
+    lib.td_segment_hash.argtypes = [VP, I64]
+    lib.td_segment_hash.restype = C.c_uint64
     lib.td_status_string.argtypes = [C.c_int]
     lib.td_status_string.restype = C.c_char_p
     return lib
@@ -95,7 +107,8 @@ _lib = _load()
 EXPORTS = ("td_ctx_create", "td_ctx_destroy", "td_status_string", "td_round_offsets",
            "td_rerotate_batched", "td_check_select", "td_pick_master", "td_diff_encode",
            "td_fused_restore", "td_get_error", "td_check_select_noalloc",
-           "td_check_select_group", "td_pick_master_min_deviation")
+           "td_check_select_group", "td_pick_master_min_deviation", "td_segment_hash",
+           "td_form_rounds", "td_group_round")
 
 
 def lib_path() -> str:
@@ -201,6 +214,59 @@ def td_pick_master_min_deviation(ctx, rnd, sel, k, dev, score_out, master_dev, s
         _check(s, "td_pick_master_min_deviation")
         return m.value
     return s, m.value
+
+
+def _prompts(prompts, pages=None):
+    keep, arr = [], (td_prompt * max(len(prompts), 1))()
+    for r, toks in enumerate(prompts):
+        t = np.ascontiguousarray(np.asarray(toks, dtype=np.int32))
+        pg = None
+        if pages is not None and pages[r] is not None:
+            pg = np.ascontiguousarray(np.asarray(pages[r], dtype=np.int32))
+            keep.append(pg)
+        keep.append(t)
+        arr[r] = td_prompt(t.ctypes.data if t.size else None, t.size,
+                           pg.ctypes.data if pg is not None else None)
+    return arr, keep
+
+
+def td_segment_hash(tokens) -> int:
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    return int(_lib.td_segment_hash(t.ctypes.data if t.size else None, t.size))
+
+
+def td_form_rounds(prompts, sep_token, page_size, pages=None, cached_hashes=None):
+    """Returns (group_of, status_of, n_groups) as numpy arrays / int."""
+    arr, keep = _prompts(prompts, pages)
+    n = len(prompts)
+    g = np.zeros(max(n, 1), dtype=np.int32)
+    st = np.zeros(max(n, 1), dtype=np.int32)
+    ng = C.c_int32(0)
+    ch = None if cached_hashes is None else np.ascontiguousarray(np.asarray(cached_hashes, dtype=np.uint64))
+    _check(_lib.td_form_rounds(arr, n, sep_token, page_size,
+                               ch.ctypes.data if ch is not None and ch.size else None,
+                               0 if ch is None else ch.size, g.ctypes.data, st.ctypes.data,
+                               C.byref(ng)), "td_form_rounds")
+    return g[:n].copy(), st[:n].copy(), ng.value
+
+
+def td_group_round(prompts, sep_token, group_of, group, cap_members=None, cap_blocks=None):
+    """Returns (members, block_len, hist_len, perm[n_members][M])."""
+    arr, keep = _prompts(prompts)
+    n = len(prompts)
+    cm = cap_members or max(n, 1)
+    cb = cap_blocks or max(max((sum(1 for t in p if t == sep_token) for p in prompts), default=1), 1)
+    go = np.ascontiguousarray(np.asarray(group_of, dtype=np.int32))
+    mem = np.zeros(cm, np.int32)
+    bl = np.zeros(cb, np.int32)
+    hl = np.zeros(cm, np.int32)
+    pm = np.zeros(cm * cb, np.int32)
+    nm, nb = C.c_int32(0), C.c_int32(0)
+    _check(_lib.td_group_round(arr, n, sep_token, go.ctypes.data, group, cm, cb, mem.ctypes.data,
+                               C.byref(nm), bl.ctypes.data, C.byref(nb), hl.ctypes.data,
+                               pm.ctypes.data), "td_group_round")
+    m, M = nm.value, nb.value
+    return mem[:m].copy(), bl[:M].copy(), hl[:m].copy(), pm[:m * M].reshape(m, M).copy()
 
 
 def td_check_select_noalloc(shape: td_shape, rnd: td_round, check_layer, pool, k_fresh,

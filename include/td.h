@@ -263,6 +263,57 @@ td_status td_check_select_noalloc(const td_shape* shape, const td_round* round,
                                   const void* k_fresh, int32_t recompute_pct, int32_t* sel,
                                   int32_t* k_out, uint32_t* err_bits_out, void* stream);
 
+/* ---- Round-aware prompts and the KV Collector (host only) --------------------------
+ * [R] Summary Method (1): the application puts a reserved separator token ([B] §4.1:
+ * <TTSEP>) in front of every shared output block, so the runtime can hash segments by
+ * content and recognise the blocks agents share; Method (2) and §5 "Batch formation": the
+ * KV Collector groups a round's requests that share the same active prompt length, the
+ * same cached span and disjoint slot mappings, and falls back to per-request processing
+ * for the rest. A prompt is [private history][SEP block][SEP block]...: the tokens before
+ * the first separator are the history; each later segment starts at a separator, which
+ * belongs to it (block lengths tile the prompt). Two blocks are the same block when their
+ * tokens are equal (the hash only indexes; equality is checked on the tokens). */
+typedef struct td_prompt {
+  const int32_t* tokens;   /* HOST [n_tokens] */
+  int64_t n_tokens;
+  const int32_t* pages;    /* HOST physical page of each logical page of the prompt
+                              ([ceil(n_tokens / page_size)]), or NULL */
+} td_prompt;
+
+typedef enum td_round_status {
+  TD_ROUND_OK = 0,              /* joined a collective round */
+  TD_ROUND_NO_BLOCKS = 1,       /* no separator: nothing shared; runs alone */
+  TD_ROUND_REPEATED_BLOCK = 2,  /* the same block twice: not a round; runs alone */
+  TD_ROUND_NOT_CACHED = 3       /* a block without cached canonical K/V; runs alone */
+} td_round_status;
+
+/* 64-bit FNV-1a over the little-endian bytes of the tokens (the segment index key). */
+uint64_t td_segment_hash(const int32_t* tokens, int64_t n_tokens);
+
+/* Group requests into collective rounds, in arrival order. A request with at least one
+ * block, no block twice and (when cached_hashes is given) every block's td_segment_hash in
+ * cached_hashes joins the first group with exactly its set of blocks none of whose members
+ * uses a page that the request's shared span uses (pages given); otherwise it opens a new
+ * group. Other requests get a group of their own and a fallback status. Groups are
+ * numbered in order of their first member.
+ *   prompts        HOST [n_prompts]
+ *   cached_hashes  HOST [n_cached], or NULL: every block counts as cached
+ *   group_of, status_of  HOST int32 [n_prompts], outputs; n_groups_out HOST int32 */
+td_status td_form_rounds(const td_prompt* prompts, int32_t n_prompts, int32_t sep_token,
+                         int32_t page_size, const uint64_t* cached_hashes, int32_t n_cached,
+                         int32_t* group_of, int32_t* status_of, int32_t* n_groups_out);
+
+/* The round descriptor of one group: members in arrival order, blocks in the order of
+ * the first member's prompt, each member's history length and permutation (slot q of
+ * member x holds block perm[x*M + q]) - ready for td_round. All HOST; capacities in
+ * members and blocks; TD_ERR_CAPACITY when they are too small, TD_ERR_INVALID_ARG when
+ * the group's members do not hold one same set of distinct blocks. */
+td_status td_group_round(const td_prompt* prompts, int32_t n_prompts, int32_t sep_token,
+                         const int32_t* group_of, int32_t group, int32_t cap_members,
+                         int32_t cap_blocks, int32_t* members, int32_t* n_members,
+                         int32_t* block_len, int32_t* n_blocks, int32_t* hist_len,
+                         int32_t* perm);
+
 /* Synchronize the stream, read and clear the error word. Returns TD_OK when no device
  * fault was recorded, else the lowest td_status code recorded; bits_out (HOST, or NULL)
  * receives the whole word (bit c set = code c recorded). */

@@ -23,7 +23,7 @@ def td():
 def _declared():
     text = open(os.path.join(ROOT, "include", "td.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:td_status|const char\*)\s+(td_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:td_status|const char\*|uint64_t)\s+(td_\w+)\s*\(", text, re.M)))
 
 
 def test_every_declared_symbol_is_exported(td):
