@@ -134,4 +134,41 @@ cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& poo
   return go<2>(g, rd, pool, store, agents, layer_begin, store_layer0, nl, frame, err, st);
 }
 
+// The dense restore the fused restore replaces ([R] §3d; Figure 5's "dense Mirror"): one
+// agent's canonical-frame cache materialised as [layer][token][E] K and V, the Master's
+// rows with the agent's records laid over them. One CTA per (layer, diff block, K or V)
+// copies the block's rows with 16-byte loads and stores. A comparison baseline only.
+__global__ void __launch_bounds__(256)
+materialise_kernel(int E, int S, int nb, StoreDev store, int agent, int sl0,
+                   uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, uint32_t* err) {
+  const int kv = blockIdx.x & 1;
+  const int b = (blockIdx.x >> 1) % nb;
+  const int li = (blockIdx.x >> 1) / nb;
+  const int sl = sl0 + li;
+  int rec = __ldg(store.slot + (static_cast<int64_t>(agent) * store.nl + sl) * nb + b);
+  if (rec >= store.capacity) {
+    if (threadIdx.x == 0) atomicOr(err, err_bit(TD_ERR_INVALID_ARG));
+    return;
+  }
+  const int t0 = b * kDiffBlock;
+  const int ntok = min(kDiffBlock, S - t0);
+  const int vpt = E / 8;
+  const uint16_t* src = rec >= 0
+      ? (kv ? store.val_v : store.val_k) + static_cast<int64_t>(rec) * kDiffBlock * E
+      : (kv ? store.master_v : store.master_k) + (static_cast<int64_t>(sl) * S + t0) * E;
+  uint16_t* dst = (kv ? dv : dk) + (static_cast<int64_t>(li) * S + t0) * E;
+  for (int v = threadIdx.x; v < ntok * vpt; v += blockDim.x)
+    st16(dst + static_cast<int64_t>(v) * 8, ldg16(src + static_cast<int64_t>(v) * 8));
+}
+
+cudaError_t launch_materialise(const Geom& g, const RoundDev& rd, const StoreDev& store,
+                               int agent, int sl0, int nl, uint16_t* dk, uint16_t* dv,
+                               uint32_t* err, cudaStream_t st) {
+  const int64_t units = static_cast<int64_t>(nl) * rd.nb * 2;
+  if (units == 0) return cudaSuccess;
+  materialise_kernel<<<static_cast<unsigned>(units), 256, 0, st>>>(g.E, rd.S, rd.nb, store,
+                                                                   agent, sl0, dk, dv, err);
+  return cudaGetLastError();
+}
+
 }  // namespace td

@@ -568,6 +568,40 @@ td_status td_fused_restore(td_ctx* c, const td_round* r, const td_diff_store* st
   return TD_OK;
 }
 
+td_status td_materialise_mirror(td_ctx* c, const td_round* r, const td_diff_store* store,
+                                int32_t agent, int32_t layer_begin, int32_t layer_end,
+                                void* dense_k, void* dense_v, void* stream) {
+  if (!c || !same_device(c) || !store || !dense_k || !dense_v || !aligned16(dense_k) ||
+      !aligned16(dense_v))
+    return TD_ERR_INVALID_ARG;
+  if (!store->master_k || !store->master_v || !store->slot || !aligned16(store->master_k) ||
+      !aligned16(store->master_v))
+    return TD_ERR_INVALID_ARG;
+  if (layer_begin < store->layer_begin || layer_end > store->layer_end ||
+      layer_begin >= layer_end || store->layer_begin < 0 ||
+      store->layer_end > c->shape.n_layers)
+    return TD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  td_status s = prepare_round(c, r, st);
+  if (s != TD_OK) return s;
+  if (agent < 0 || agent >= c->N) return TD_ERR_INVALID_ARG;
+  StoreDev sd;
+  sd.master_k = static_cast<uint16_t*>(store->master_k);
+  sd.master_v = static_cast<uint16_t*>(store->master_v);
+  sd.rowptr = store->rowptr;
+  sd.block_idx = store->block_idx;
+  sd.val_k = static_cast<uint16_t*>(store->val_k);
+  sd.val_v = static_cast<uint16_t*>(store->val_v);
+  sd.slot = store->slot;
+  sd.capacity = store->capacity_blocks;
+  sd.nl = store->layer_end - store->layer_begin;
+  if (launch_materialise(c->g, round_dev(c), sd, agent, layer_begin - store->layer_begin,
+                         layer_end - layer_begin, static_cast<uint16_t*>(dense_k),
+                         static_cast<uint16_t*>(dense_v), c->d_err, st) != cudaSuccess)
+    return TD_ERR_CUDA;
+  return TD_OK;
+}
+
 td_status td_get_error(td_ctx* c, void* stream, uint32_t* bits_out) {
   if (!c || !same_device(c)) return TD_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

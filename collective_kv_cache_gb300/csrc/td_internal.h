@@ -123,4 +123,8 @@ cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& poo
                            int store_layer0, int nl, int frame, uint32_t* err,
                            cudaStream_t st);
 
+cudaError_t launch_materialise(const Geom& g, const RoundDev& rd, const StoreDev& store,
+                               int agent, int sl0, int nl, uint16_t* dk, uint16_t* dv,
+                               uint32_t* err, cudaStream_t st);
+
 }  // namespace td

@@ -43,6 +43,7 @@ class RoundRunner:
         self.ctx = td.Context(td.make_shape(cfg), max_agents or self.N, max_blocks or self.M,
                               max_shared or self.S)
         self.round = td.make_round(block_len, hist_len, perm)
+        self._views = None
         self.num_pages = int(num_pages)
         shape = (self.L, 2, self.num_pages, cfg.page_size, cfg.n_kv_heads, cfg.head_dim)
         if pool_fill is None:
@@ -161,6 +162,47 @@ class RoundRunner:
 
     def get_error(self):
         return td.td_get_error(self.ctx.handle, self.s)
+
+    # ------------------------------------------------------------------ comparison baselines
+    def agent_views(self):
+        """Each agent as a round of its own (its history, its block order, its row of the
+        block table) on the same pool: what a per-request system sees."""
+        if self._views is None:
+            bl, hl, pm = self.round._keep
+            pm = pm.reshape(self.N, self.M)
+            self._views = []
+            for i in range(self.N):
+                ctx = td.Context(td.make_shape(self.cfg), 1, self.M, self.S)
+                self._views.append((ctx, td.make_round(bl, hl[i:i + 1], pm[i:i + 1]),
+                                    td.make_paged(self.pool_t, self.bt_t[i:i + 1])))
+        return self._views
+
+    def serial_pic(self, kc, vc, k_fresh):
+        """Per-request position-independent caching: for every agent in turn, re-rotate
+        the shared blocks into its pages (re-reading the canonical K/V) and run its own
+        check-layer selection. Selections land in the rows of sel_t / dev_t."""
+        pct, c = self.cfg.recompute_pct, self.cfg.check_layer
+        k = (pct * self.S + 99) // 100
+        if self.sel_t is None or self.sel_t.shape[1] != k:
+            self.sel_t = torch.zeros((self.N, max(k, 0)), dtype=torch.int32, device=self.device)
+        for i, (ctx, rnd, pool) in enumerate(self.agent_views()):
+            td.td_rerotate_batched(ctx.handle, rnd, kc.data_ptr(), vc.data_ptr(), 0, self.L,
+                                   pool, self.s)
+            td.td_check_select(ctx.handle, rnd, c, pool, k_fresh[i].data_ptr(), pct,
+                               self.sel_t[i].data_ptr() if k else None, self.dev_t[i].data_ptr(),
+                               self.s)
+
+    def dense_restore(self, agents: Sequence[int], dense_k: torch.Tensor, dense_v: torch.Tensor):
+        """Restore by materialising each agent's dense cache ([L][S][E] K and V), then
+        re-rotating it into the agent's pages: the path the fused restore replaces."""
+        views = self.agent_views()
+        lb, le = self.store.layer_begin, self.store.layer_end
+        for a in agents:
+            td.td_materialise_mirror(self.ctx.handle, self.round, self.store, a, lb, le,
+                                     dense_k.data_ptr(), dense_v.data_ptr(), self.s)
+            ctx, rnd, pool = views[a]
+            td.td_rerotate_batched(ctx.handle, rnd, dense_k.data_ptr(), dense_v.data_ptr(), lb,
+                                   le, pool, self.s)
 
     # ------------------------------------------------------------------ helpers for inputs
     def positions(self) -> np.ndarray:

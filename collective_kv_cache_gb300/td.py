@@ -88,6 +88,7 @@ def _load() -> C.CDLL:
         "td_check_select_group": [VP, P(td_round), I32, P(td_paged), VP, I32, VP, VP, VP,
                                   P(I32), VP],
         "td_pick_master_min_deviation": [VP, P(td_round), VP, I32, VP, VP, VP, P(I32), VP],
+        "td_materialise_mirror": [VP, P(td_round), P(td_diff_store), I32, I32, I32, VP, VP, VP],
         "td_form_rounds": [P(td_prompt), I32, I32, I32, VP, I32, VP, VP, P(I32)],
         "td_group_round": [P(td_prompt), I32, I32, VP, I32, I32, I32, VP, P(I32), VP, P(I32),
                            VP, VP],
@@ -108,7 +109,7 @@ EXPORTS = ("td_ctx_create", "td_ctx_destroy", "td_status_string", "td_round_offs
            "td_rerotate_batched", "td_check_select", "td_pick_master", "td_diff_encode",
            "td_fused_restore", "td_get_error", "td_check_select_noalloc",
            "td_check_select_group", "td_pick_master_min_deviation", "td_segment_hash",
-           "td_form_rounds", "td_group_round")
+           "td_form_rounds", "td_group_round", "td_materialise_mirror")
 
 
 def lib_path() -> str:
@@ -214,6 +215,13 @@ def td_pick_master_min_deviation(ctx, rnd, sel, k, dev, score_out, master_dev, s
         _check(s, "td_pick_master_min_deviation")
         return m.value
     return s, m.value
+
+
+def td_materialise_mirror(ctx, rnd, store, agent, layer_begin, layer_end, dense_k, dense_v,
+                          stream=0) -> int:
+    return _check(_lib.td_materialise_mirror(ctx, C.byref(rnd), C.byref(store), agent,
+                                             layer_begin, layer_end, dense_k, dense_v, stream),
+                  "td_materialise_mirror")
 
 
 def _prompts(prompts, pages=None):

@@ -263,6 +263,19 @@ td_status td_check_select_noalloc(const td_shape* shape, const td_round* round,
                                   const void* k_fresh, int32_t recompute_pct, int32_t* sel,
                                   int32_t* k_out, uint32_t* err_bits_out, void* stream);
 
+/* Comparison baseline, not on the path: the dense restore that td_fused_restore replaces
+ * ([R] §3d and Figure 5: materialise the Mirror, then copy it into pages). Writes agent's
+ * canonical-frame cache X_agent for layers [layer_begin, layer_end): the Master's rows
+ * with the agent's records laid over them (the Master itself: the Master's rows).
+ * dense_k, dense_v: DEVICE bf16 [layer_end-layer_begin][S][E], caller-owned, 16-byte
+ * aligned. Following it with td_rerotate_batched of a one-agent round (the agent's
+ * history and order, its block-table row) reproduces td_fused_restore's frame-0 pages.
+ * A slot map entry beyond the store's capacity sets TD_ERR_INVALID_ARG in the error word
+ * and leaves that block unwritten. */
+td_status td_materialise_mirror(td_ctx* ctx, const td_round* round, const td_diff_store* store,
+                                int32_t agent, int32_t layer_begin, int32_t layer_end,
+                                void* dense_k, void* dense_v, void* stream);
+
 /* ---- Round-aware prompts and the KV Collector (host only) --------------------------
  * [R] Summary Method (1): the application puts a reserved separator token ([B] §4.1:
  * <TTSEP>) in front of every shared output block, so the runtime can hash segments by

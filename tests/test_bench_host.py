@@ -6,6 +6,7 @@ from __future__ import annotations
 import os
 import socket
 
+import numpy as np
 import pytest
 
 import bench
@@ -77,3 +78,22 @@ def test_two_rank_gloo_reductions():
     assert [o[1] for o in out] == [15.0, 15.0]          # max over ranks
     assert [o[2] for o in out] == [300.0, 300.0]        # whole-job work
     assert out[0][3] != out[1][3]                        # independent rounds
+
+
+def test_threaded_oracle_baseline_matches_single_threaded():
+    """The threaded CPU baseline runs the same oracle calls split over layers and agents:
+    same selection size and number of diff blocks, and the same restored pool."""
+    import bench
+    import oracle
+    from collective_kv_cache_gb300 import synth
+    cfg = synth.tiny().replace(n_layers=4, check_layer=1)
+    sub, rnd, kc, vc, orc = bench.oracle_round(cfg, cfg.seed, cfg.n_layers)
+    cache = {}
+    _, k, nnz = bench.oracle_step(sub, rnd, kc, vc, orc, cache)
+    single = cache["restored"]
+    _, k_t, nnz_t = bench.oracle_step_threaded(sub, rnd, kc, vc, orc, cache, threads=3)
+    cache["executor"].shutdown()
+    assert (k_t, nnz_t) == (k, nnz) and nnz > 0
+    assert np.array_equal(cache["restored"], single)
+    out = bench.cpu_baseline(cfg, cfg.seed, min_seconds=0.0, max_passes=1)
+    assert out["threaded"]["value"] > 0 and out["threaded"]["cores"] >= 1
