@@ -210,15 +210,26 @@ def setup_round(cfg, seed, device, store_on_host=False):
 
 
 def workload_config(name: str):
-    """qwen7b, qwen14b, scale64, tiny, or density<pct>[_p<page>] (e.g. density40_p32)."""
+    """qwen7b, qwen14b, scale64, tiny or density<pct>, optionally followed by _p<page size>
+    and _b<diff block> (e.g. density40_p32, qwen7b_p32_b32: diff block = page size)."""
     from collective_kv_cache_gb300 import synth
-    if name in synth.CONFIGS:
-        return synth.CONFIGS[name]()
-    if name.startswith("density"):
-        body = name[len("density"):]
-        pct, _, page = body.partition("_p")
-        return synth.density(int(pct), page_size=int(page) if page else 16)
-    raise SystemExit(f"unknown workload {name}")
+    base, *opts = name.split("_")
+    kw = {}
+    for o in opts:
+        if o[:1] in ("p", "b") and o[1:].isdigit():
+            kw["page_size" if o[0] == "p" else "diff_block"] = int(o[1:])
+        else:
+            raise SystemExit(f"unknown workload {name}")
+    if base in synth.CONFIGS:
+        cfg = synth.CONFIGS[base]()
+    elif base.startswith("density") and base[len("density"):].isdigit():
+        cfg = synth.density(int(base[len("density"):]), page_size=kw.pop("page_size", 16))
+        opts = [o for o in opts if o[0] != "p"]
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    if kw:
+        cfg = cfg.replace(**kw, name=cfg.name + "".join(f"_{o}" for o in opts))
+    return cfg
 
 
 def bench_chunked(args, cfg, seed, device):
@@ -436,9 +447,9 @@ def bench_ours(args, rank, world, local_rank):
             "diff_blocks": st["nnz"], "selected_per_agent": st["k"], "master": st["master"],
             "host_link": None if not args.store_on_host else {
                 "restore_reads_gbs": round((2 * L * cfg.n_shared * cfg.elems * 2 + st["nnz"] *
-                                            (16 * cfg.elems * 4 + 4)) / (stage_ms["restore"] * 1e-3) / 1e9, 1),
+                                            (cfg.diff_block * cfg.elems * 4 + 4)) / (stage_ms["restore"] * 1e-3) / 1e9, 1),
                 "encode_writes_gbs": round((2 * L * cfg.n_shared * cfg.elems * 2 + st["nnz"] *
-                                            (16 * cfg.elems * 4 + 4)) / (stage_ms["encode"] * 1e-3) / 1e9, 1)},
+                                            (cfg.diff_block * cfg.elems * 4 + 4)) / (stage_ms["encode"] * 1e-3) / 1e9, 1)},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": traffic, "peak_kind": peak_kind},

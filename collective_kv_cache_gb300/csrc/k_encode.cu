@@ -8,16 +8,17 @@
 // are mask_i | mask_master. Their number per layer is known before any K/V is read, which
 // gives every candidate block a fixed place in the store. Three launches:
 //   prep    one CTA per agent: zeroes the agent's flags and record counts, builds a
-//           16-bit mask of its selected tokens in each diff block, the rank of the
+//           mask of its selected tokens in each diff block (16 or 32 bits), the rank of the
 //           block's first selected token and its block bitmask; the CTA that finishes
 //           last (a self-resetting counter; no CTA waits) builds the candidate masks, the
 //           per-word and per-agent prefix counts, the bound nl * sum_i |cand_i|, and
 //           checks the master
-//   main    one CTA per (layer, 16-token block, K or V, part): reads its canonical data
+//   main    one CTA per (layer, 16-token tile, K or V, part), the tiles covering whole
+//           diff blocks (a 32-token block is two tiles): reads its canonical data
 //           once, builds the Master's (recomputed K turned back by R(-off)) and writes it,
 //           then for each candidate Mirror builds its data, writes it at its candidate
 //           place and ORs "differs" into the block's flag, one atomic per warp; the warp
-//           that sets a flag first counts the record in its row. One CTA per tile writes
+//           that sets a flag first counts the record in its row. One CTA per block writes
 //           the slot map and block indices of the common case (every candidate kept);
 //           the CTA that finishes last turns the record counts into rowptr.
 //   fixup   only when some candidate equalled the Master's block: compacts the slot map
@@ -116,9 +117,9 @@ __global__ void __launch_bounds__(1024) enc_prep_kernel(EncArgs a, const int32_t
       atomicOr(a.err, err_bit(TD_ERR_INVALID_ARG));
       continue;
     }
-    const int b = t / kDiffBlock;
-    atomicOr(&bits[b], 1u << (t - b * kDiffBlock));
-    if (prev < 0 || prev / kDiffBlock != b) first[b] = r;
+    const int b = t / a.rd.B;
+    atomicOr(&bits[b], 1u << (t - b * a.rd.B));
+    if (prev < 0 || prev / a.rd.B != b) first[b] = r;
     atomicOr(&smask[b >> 5], 1u << (b & 31));
   }
   __syncthreads();
@@ -176,10 +177,11 @@ __device__ void rows_prefix(const EncArgs& a) {
   }
 }
 
-// Per-thread items of one half-tile (K or V) of a (layer, block) tile.
+// Per-thread items of one half-tile (K or V) of a (layer, 16-token tile) unit.
 template <int kItems>
 struct HalfTile {
-  int tl[kItems];     // token within the block
+  int tl[kItems];     // token within the tile
+  int tb[kItems];     // row within the diff block (the tile's first row tb0 + tl)
   int e0[kItems];
   int f0[kItems];
   int blk[kItems];
@@ -189,9 +191,9 @@ struct HalfTile {
 };
 
 template <int kItems>
-__device__ __forceinline__ void load_half(const EncArgs& a, int li, int t0, int kv, int q0,
-                                          HalfTile<kItems>& h) {
-  const int n_items = kDiffBlock * a.g.vpt;
+__device__ __forceinline__ void load_half(const EncArgs& a, int li, int t0, int tb0, int kv,
+                                          int q0, HalfTile<kItems>& h) {
+  const int n_items = kTile * a.g.vpt;
   const uint16_t* src = kv == 0 ? a.kc : a.vc;
 #pragma unroll
   for (int r = 0; r < kItems; ++r) {
@@ -199,6 +201,7 @@ __device__ __forceinline__ void load_half(const EncArgs& a, int li, int t0, int 
     const Item it = item_of(a.g, q < n_items ? q : 0);
     const int t = t0 + it.tok;
     h.tl[r] = it.tok;
+    h.tb[r] = tb0 + it.tok;
     h.e0[r] = it.e0;
     h.f0[r] = it.f0;
     h.live[r] = q < n_items && t < a.rd.S;
@@ -222,8 +225,8 @@ __device__ __forceinline__ void agent_item(const EncArgs& a, int ag, int li, int
                                            int r, uint4& x0, uint4& x1) {
   x0 = h.c0[r];
   x1 = h.c1[r];
-  if (!((sbits >> h.tl[r]) & 1u)) return;
-  const int rk = first + __popc(sbits & ((1u << h.tl[r]) - 1u));
+  if (!((sbits >> h.tb[r]) & 1u)) return;
+  const int rk = first + __popc(sbits & ((1u << h.tb[r]) - 1u));
   const int64_t row = ((static_cast<int64_t>(ag) * a.nl + li) * a.k + rk) * a.g.E;
   if (kv == 0) {
     const uint4 fa = ldg16(a.kf + row + h.e0[r]);
@@ -241,7 +244,7 @@ __device__ __forceinline__ void store_item(const EncArgs& a, int kv, int64_t rec
                                            const HalfTile<kItems>& h, int r, const uint4& x0,
                                            const uint4& x1) {
   uint16_t* dst = (kv == 0 ? a.store.val_k : a.store.val_v) +
-                  (rec * kDiffBlock + h.tl[r]) * a.g.E;
+                  (rec * a.rd.B + h.tb[r]) * a.g.E;
   st16(dst + h.e0[r], x0);
   st16(dst + h.e0[r] + a.g.half, x1);
 }
@@ -270,8 +273,8 @@ __device__ __forceinline__ void stage_candidate(const EncArgs& a, int ag, int li
   const uint16_t* src = kv == 0 ? a.kf : a.vf;
 #pragma unroll
   for (int r = 0; r < kItems; ++r) {
-    if (!h.live[r] || !((sbits >> h.tl[r]) & 1u)) continue;
-    const int rk = first + __popc(sbits & ((1u << h.tl[r]) - 1u));
+    if (!h.live[r] || !((sbits >> h.tb[r]) & 1u)) continue;
+    const int rk = first + __popc(sbits & ((1u << h.tb[r]) - 1u));
     const uint16_t* row = src + ((static_cast<int64_t>(ag) * a.nl + li) * a.k + rk) * a.g.E;
     cp_async16(slot + (0 * kItems + r) * blockDim.x + threadIdx.x, row + h.e0[r]);
     cp_async16(slot + (1 * kItems + r) * blockDim.x + threadIdx.x, row + h.e0[r] + a.g.half);
@@ -286,7 +289,7 @@ __device__ __forceinline__ void staged_item(const EncArgs& a, int ag, int kv, un
                                             const uint4* slot, uint4& x0, uint4& x1) {
   x0 = h.c0[r];
   x1 = h.c1[r];
-  if (!((sbits >> h.tl[r]) & 1u)) return;
+  if (!((sbits >> h.tb[r]) & 1u)) return;
   const uint4 fa = slot[(0 * kItems + r) * blockDim.x + threadIdx.x];
   const uint4 fb = slot[(1 * kItems + r) * blockDim.x + threadIdx.x];
   if (kv == 0) {
@@ -304,13 +307,15 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
   if (m < 0) return;
   const int over = *a.over;
   const Unit un = unit_of(a.g, blockIdx.x, tiles_per_layer);
-  const int kv = un.kv, li = un.li, b = un.b;
-  const int t0 = b * kDiffBlock;
+  const int kv = un.kv, li = un.li;
+  const int t0 = un.b * kTile;
+  const int b = t0 / a.rd.B;                 // the tile's diff block
+  const int tb0 = t0 - b * a.rd.B;           // the tile's first row within it
   const int N = a.rd.N, nb = a.rd.nb, nbw = a.sc.nbw;
   const int lane = threadIdx.x & 31;
 
   HalfTile<kItems> h;
-  load_half<kItems>(a, li, t0, kv, un.q0, h);
+  load_half<kItems>(a, li, t0, tb0, kv, un.q0, h);
 
   // the Master's half-tile, written dense
   const unsigned mbits = a.sc.selbits[static_cast<int64_t>(m) * nb + b];
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
     st16(mdst + row + h.e0[r] + a.g.half, m1[r]);
   }
 
-  const bool designated = kv == 0 && un.q0 == 0;   // one CTA per tile writes slot/index
+  const bool designated = kv == 0 && un.q0 == 0 && tb0 == 0;  // one CTA per block: slot/index
   // per-agent facts of this block, one chunk of agents at a time
   __shared__ int64_t s_place[kAgentChunk];   // candidate place, -1 = not a candidate
   __shared__ unsigned s_bits[kAgentChunk];
@@ -466,9 +471,11 @@ __global__ void __launch_bounds__(256) enc_fixup_kernel(EncArgs a, int tiles_per
   const int64_t units = static_cast<int64_t>(tiles_per_layer) * a.nl * 2 * parts_per_tile(a.g);
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const Unit un = unit_of(a.g, u, tiles_per_layer);
-    const int kv = un.kv, li = un.li, b = un.b;
+    const int kv = un.kv, li = un.li;
+    const int t0 = un.b * kTile;
+    const int b = t0 / a.rd.B;
     HalfTile<kItems> h;
-    load_half<kItems>(a, li, b * kDiffBlock, kv, un.q0, h);
+    load_half<kItems>(a, li, t0, t0 - b * a.rd.B, kv, un.q0, h);
     for (int i = 0; i < a.rd.N; ++i) {
       if (i == m) continue;
       const int64_t row = static_cast<int64_t>(i) * a.nl + li;
@@ -496,7 +503,7 @@ __global__ void __launch_bounds__(256) enc_fixup_kernel(EncArgs a, int tiles_per
 
 template <int kItems>
 static cudaError_t run_tiles(const EncArgs& a, int threads, cudaStream_t st) {
-  const int tpl = a.rd.nb;
+  const int tpl = a.rd.nb * (a.rd.B / kTile);   // whole diff blocks: tails are zeroed
   const int64_t units = static_cast<int64_t>(tpl) * a.nl * 2 * parts_per_tile(a.g);
   // the staging ring: kStageDepth candidates x 2 vectors x kItems per thread (48 KiB at
   // 256 threads and two items); beyond the default window, so opt in (once per device)

@@ -2,8 +2,8 @@
 // agent with the smallest deviation as the dense Master; §3c A2: the deviation score is
 // chosen so that the Mirrors' diffs come out sparsest).
 //
-// One CTA per agent turns the agent's selection into a bitmask over the 16-token diff
-// blocks; the CTA that finishes last (a self-resetting counter; no CTA waits) gathers the
+// One CTA per agent turns the agent's selection into a bitmask over the diff blocks (16
+// or 32 tokens); the CTA that finishes last (a self-resetting counter; no CTA waits) gathers the
 // masks and counts cost(m) = sum over i != m of popcount(mask_i | mask_m), one warp per
 // candidate m; the smallest cost wins, ties to the lower index. Integer arithmetic only,
 // so the result does not depend on the order of the additions.
@@ -12,7 +12,7 @@
 namespace td {
 
 __global__ void __launch_bounds__(1024)
-pick_master_kernel(const int32_t* __restrict__ sel, int N, int S, int k, int nbw,
+pick_master_kernel(const int32_t* __restrict__ sel, int N, int S, int B, int k, int nbw,
                    int64_t* __restrict__ cost_out, int32_t* __restrict__ master,
                    uint32_t* gmask, int* done, uint32_t* err) {
   extern __shared__ unsigned char smem_raw[];
@@ -32,7 +32,7 @@ pick_master_kernel(const int32_t* __restrict__ sel, int N, int S, int k, int nbw
     if (x < k) {
       const int t = __ldg(row + x);
       if (t < 0 || t >= S) atomicOr(err, err_bit(TD_ERR_INVALID_ARG));
-      else b = t / kDiffBlock;
+      else b = t / B;
     }
     const int prev = __shfl_up_sync(0xFFFFFFFFu, b, 1);
     if (b >= 0 && (lane == 0 || prev != b)) atomicOr(&mask[b >> 5], 1u << (b & 31));
@@ -75,10 +75,10 @@ pick_master_kernel(const int32_t* __restrict__ sel, int N, int S, int k, int nbw
   }
 }
 
-cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int k, int64_t* cost,
+cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int B, int k, int64_t* cost,
                                int32_t* master, uint32_t* gmask, int* done, uint32_t* err,
                                cudaStream_t st) {
-  const int nb = (S + kDiffBlock - 1) / kDiffBlock;
+  const int nb = (S + B - 1) / B;
   const int nbw = (nb + 31) / 32;
   const size_t smem = ((static_cast<size_t>(N) * nbw * 4 + 7) & ~size_t(7)) + 8 * static_cast<size_t>(N);
   if (smem > 48 * 1024) {
@@ -88,7 +88,7 @@ cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int k, int64_t*
     if (e != cudaSuccess) return e;
   }
   const int threads = k >= 512 ? 1024 : 256;
-  pick_master_kernel<<<N, threads, smem, st>>>(sel, N, S, k, nbw, cost, master, gmask, done,
+  pick_master_kernel<<<N, threads, smem, st>>>(sel, N, S, B, k, nbw, cost, master, gmask, done,
                                                err);
   return cudaGetLastError();
 }

@@ -16,13 +16,13 @@ __global__ void __launch_bounds__(256, 4)
 rerotate_kernel(Geom g, RoundDev rd, PoolDev pool, const uint16_t* __restrict__ kc,
                 const uint16_t* __restrict__ vc, int layer_begin, int tiles_per_layer,
                 uint32_t* err) {
-  __shared__ int64_t s_row[kAgentChunk * kDiffBlock];  // pool row of (agent, token)
+  __shared__ int64_t s_row[kAgentChunk * kTile];  // pool row of (agent, token)
   const Unit un = unit_of(g, blockIdx.x, tiles_per_layer);
   if (un.kv == 1 && vc == nullptr) return;
   const uint16_t* src = un.kv == 0 ? kc : vc;
-  const int t0 = un.b * kDiffBlock;
+  const int t0 = un.b * kTile;
   const int layer = layer_begin + un.li;
-  const int n_items = kDiffBlock * g.vpt;
+  const int n_items = kTile * g.vpt;
 
   uint4 xa[kItems], xb[kItems];
   int e0[kItems], f0[kItems], tl[kItems], blk[kItems];
@@ -55,7 +55,7 @@ rerotate_kernel(Geom g, RoundDev rd, PoolDev pool, const uint16_t* __restrict__ 
 #pragma unroll
       for (int r = 0; r < kItems; ++r) {
         if (!live[r]) continue;
-        const int64_t row = s_row[x * kDiffBlock + tl[r]];
+        const int64_t row = s_row[x * kTile + tl[r]];
         if (row < 0) continue;
         uint16_t* dst = pool.base + row * g.E;
         if (un.kv == 0) {
@@ -74,12 +74,12 @@ rerotate_kernel(Geom g, RoundDev rd, PoolDev pool, const uint16_t* __restrict__ 
 }
 
 int tile_threads(const Geom& g) {
-  const int items = kDiffBlock * g.vpt < kPartItems ? kDiffBlock * g.vpt : kPartItems;
+  const int items = kTile * g.vpt < kPartItems ? kTile * g.vpt : kPartItems;
   return items < 256 ? items : 256;
 }
 
 int tile_items(const Geom& g) {
-  const int items = kDiffBlock * g.vpt < kPartItems ? kDiffBlock * g.vpt : kPartItems;
+  const int items = kTile * g.vpt < kPartItems ? kTile * g.vpt : kPartItems;
   const int t = tile_threads(g);
   return (items + t - 1) / t;
 }
@@ -87,7 +87,7 @@ int tile_items(const Geom& g) {
 cudaError_t launch_rerotate(const Geom& g, const RoundDev& rd, const PoolDev& pool,
                             const uint16_t* kc, const uint16_t* vc, int layer_begin, int nl,
                             uint32_t* err, cudaStream_t st) {
-  const int tpl = (rd.S + kDiffBlock - 1) / kDiffBlock;
+  const int tpl = (rd.S + kTile - 1) / kTile;
   const int64_t units = static_cast<int64_t>(tpl) * nl * 2 * parts_per_tile(g);
   if (units == 0) return cudaSuccess;
   if (tile_items(g) == 1)

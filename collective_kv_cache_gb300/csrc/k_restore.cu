@@ -3,10 +3,10 @@
 // without building a dense Mirror; §2a "Fused restore: Master chunk + diff -> paged KV";
 // §3d: recovery belongs in the transfer path, written through the paged-KV slot map).
 //
-// One CTA per unit = (layer, one 16-token diff block, K or V, part). The Master's data of
-// the unit is read from HBM once and held in registers; for each listed agent the slot
-// map says whether that agent has a record for this (layer, block): if so its record
-// replaces the Master's data for this agent only. K is turned by the agent's block
+// One CTA per unit = (layer, one 16-token tile, K or V, part). The Master's data of the
+// unit is read from HBM once and held in registers; for each listed agent the slot map
+// says whether that agent has a record for the tile's diff block (16 or 32 tokens) in
+// this layer: if so the record's rows replace the Master's data for this agent only. K is turned by the agent's block
 // offsets (frame 0) or copied (frame 1), V is copied; 16-byte stores into the agent's
 // page.
 #include "td_device.cuh"
@@ -17,13 +17,15 @@ template <int kItems, bool kRotate>
 __global__ void __launch_bounds__(256, 3)
 restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agents,
                int layer_begin, int store_layer0, int tiles_per_layer, uint32_t* err) {
-  __shared__ int64_t s_row[kAgentChunk * kDiffBlock];  // pool row of (agent, token)
-  __shared__ int s_rec[kAgentChunk];                    // record of (agent), -1 none, -2 bad
+  __shared__ int64_t s_row[kAgentChunk * kTile];  // pool row of (agent, token)
+  __shared__ int s_rec[kAgentChunk];               // record of (agent), -1 none, -2 bad
   const Unit un = unit_of(g, blockIdx.x, tiles_per_layer);
-  const int t0 = un.b * kDiffBlock;
+  const int t0 = un.b * kTile;
+  const int db = t0 / rd.B;                        // the tile's diff block
+  const int tb0 = t0 - db * rd.B;                  // the tile's first row within it
   const int layer = layer_begin + un.li;
   const int sl = layer - store_layer0;              // layer index within the store
-  const int n_items = kDiffBlock * g.vpt;
+  const int n_items = kTile * g.vpt;
   const uint16_t* master = un.kv == 0 ? store.master_k : store.master_v;
   const uint16_t* vals = un.kv == 0 ? store.val_k : store.val_v;
 
@@ -55,7 +57,7 @@ restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agen
                err);
     for (int x = threadIdx.x; x < n; x += blockDim.x) {
       const int a = agents.a[c0 + x];
-      int rec = __ldg(store.slot + (static_cast<int64_t>(a) * store.nl + sl) * rd.nb + un.b);
+      int rec = __ldg(store.slot + (static_cast<int64_t>(a) * store.nl + sl) * rd.nb + db);
       if (rec >= store.capacity) {  // a slot map that does not belong to this store
         atomicOr(err, err_bit(TD_ERR_INVALID_ARG));
         rec = -2;
@@ -73,7 +75,7 @@ restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agen
         na[r] = ma[r];
         nb[r] = mb[r];
         if (live[r] && rec >= 0) {
-          const int64_t row = (static_cast<int64_t>(rec) * kDiffBlock + tl[r]) * g.E;
+          const int64_t row = (static_cast<int64_t>(rec) * rd.B + tb0 + tl[r]) * g.E;
           na[r] = ldg16(vals + row + e0[r]);
           nb[r] = ldg16(vals + row + e0[r] + g.half);
         }
@@ -94,7 +96,7 @@ restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agen
 #pragma unroll
       for (int r = 0; r < kItems; ++r) {
         if (!live[r]) continue;
-        const int64_t row = s_row[x * kDiffBlock + tl[r]];
+        const int64_t row = s_row[x * kTile + tl[r]];
         if (row < 0) continue;
         uint16_t* dst = pool.base + row * g.E;
         uint4 sa = ca[r], sb = cb[r];
@@ -113,7 +115,7 @@ template <int kItems>
 static cudaError_t go(const Geom& g, const RoundDev& rd, const PoolDev& pool,
                       const StoreDev& store, const AgentList& agents, int layer_begin,
                       int store_layer0, int nl, int frame, uint32_t* err, cudaStream_t st) {
-  const int tpl = rd.nb;
+  const int tpl = rd.nt;
   const int64_t units = static_cast<int64_t>(tpl) * nl * 2 * parts_per_tile(g);
   if (units == 0 || agents.n == 0) return cudaSuccess;
   if (frame == 0)
@@ -139,7 +141,7 @@ cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& poo
 // rows with the agent's records laid over them. One CTA per (layer, diff block, K or V)
 // copies the block's rows with 16-byte loads and stores. A comparison baseline only.
 __global__ void __launch_bounds__(256)
-materialise_kernel(int E, int S, int nb, StoreDev store, int agent, int sl0,
+materialise_kernel(int E, int S, int B, int nb, StoreDev store, int agent, int sl0,
                    uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, uint32_t* err) {
   const int kv = blockIdx.x & 1;
   const int b = (blockIdx.x >> 1) % nb;
@@ -150,11 +152,11 @@ materialise_kernel(int E, int S, int nb, StoreDev store, int agent, int sl0,
     if (threadIdx.x == 0) atomicOr(err, err_bit(TD_ERR_INVALID_ARG));
     return;
   }
-  const int t0 = b * kDiffBlock;
-  const int ntok = min(kDiffBlock, S - t0);
+  const int t0 = b * B;
+  const int ntok = min(B, S - t0);
   const int vpt = E / 8;
   const uint16_t* src = rec >= 0
-      ? (kv ? store.val_v : store.val_k) + static_cast<int64_t>(rec) * kDiffBlock * E
+      ? (kv ? store.val_v : store.val_k) + static_cast<int64_t>(rec) * B * E
       : (kv ? store.master_v : store.master_k) + (static_cast<int64_t>(sl) * S + t0) * E;
   uint16_t* dst = (kv ? dv : dk) + (static_cast<int64_t>(li) * S + t0) * E;
   for (int v = threadIdx.x; v < ntok * vpt; v += blockDim.x)
@@ -166,7 +168,7 @@ cudaError_t launch_materialise(const Geom& g, const RoundDev& rd, const StoreDev
                                uint32_t* err, cudaStream_t st) {
   const int64_t units = static_cast<int64_t>(nl) * rd.nb * 2;
   if (units == 0) return cudaSuccess;
-  materialise_kernel<<<static_cast<unsigned>(units), 256, 0, st>>>(g.E, rd.S, rd.nb, store,
+  materialise_kernel<<<static_cast<unsigned>(units), 256, 0, st>>>(g.E, rd.S, rd.B, rd.nb, store,
                                                                    agent, sl0, dk, dv, err);
   return cudaGetLastError();
 }

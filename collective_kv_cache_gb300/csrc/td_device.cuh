@@ -77,7 +77,7 @@ __device__ __forceinline__ void rotate_pairs(const uint4& a, const uint4& b, con
   yb = pack8(y1);
 }
 
-// ---- Tile geometry: a tile is (layer, 16 canonical tokens); item q of a tile is the
+// ---- Tile geometry: a tile is (layer, kTile = 16 canonical tokens); item q of a tile is the
 // pair-vector g = q % vpt of token q / vpt. Element offsets within the token row:
 //   e0 = h*D + fg*8 (first half of head h), e1 = e0 + D/2, with h = g / (D/16),
 //   fg = g % (D/16); the table offset of the item is fg*8.
@@ -98,20 +98,20 @@ __device__ __forceinline__ Item item_of(const Geom& g, int q) {
   return it;
 }
 
-// ---- Work units of the tile kernels: (layer, diff block, K or V, part). A part covers at
+// ---- Work units of the tile kernels: (layer, 16-token tile, K or V, part). A part covers at
 // most kPartItems pair-vectors of the tile (two per thread at 256 threads), so E up to
 // 2048 never needs more than two items per thread.
 constexpr int kPartItems = 512;
 
 struct Unit {
   int li;     // layer index within the launch
-  int b;      // diff block
+  int b;      // tile (tokens b*16 .. b*16+15)
   int kv;     // 0 = K, 1 = V
   int q0;     // first item of the part
 };
 
 __host__ __device__ __forceinline__ int parts_per_tile(const Geom& g) {
-  return (kDiffBlock * g.vpt + kPartItems - 1) / kPartItems;
+  return (kTile * g.vpt + kPartItems - 1) / kPartItems;
 }
 
 __device__ __forceinline__ Unit unit_of(const Geom& g, int64_t idx, int tiles_per_layer) {
@@ -151,9 +151,9 @@ template <typename AgentOf>
 __device__ __forceinline__ void chunk_rows(const RoundDev& rd, const PoolDev& pool, int layer,
                                            int kv, int t0, int n, AgentOf agent_of,
                                            int64_t* s_row, uint32_t* err) {
-  for (int idx = threadIdx.x; idx < n * kDiffBlock; idx += blockDim.x) {
-    const int x = idx / kDiffBlock;
-    const int t = t0 + (idx - x * kDiffBlock);
+  for (int idx = threadIdx.x; idx < n * kTile; idx += blockDim.x) {
+    const int x = idx / kTile;
+    const int t = t0 + (idx - x * kTile);
     int64_t row = -1;
     if (t < rd.S) {
       const int a = agent_of(x);

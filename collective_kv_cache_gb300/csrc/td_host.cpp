@@ -190,7 +190,9 @@ RoundDev round_dev(const td_ctx* c) {
   rd.N = c->N;
   rd.M = c->M;
   rd.S = c->S;
-  rd.nb = (c->S + kDiffBlock - 1) / kDiffBlock;
+  rd.B = c->shape.diff_block;
+  rd.nb = (c->S + rd.B - 1) / rd.B;
+  rd.nt = (c->S + kTile - 1) / kTile;
   rd.off = c->d_off;
   rd.cos_t = c->d_cos;
   rd.sin_t = c->d_sin;
@@ -244,7 +246,7 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   *out = nullptr;
   const td_shape& s = *shape;
   if (s.n_layers < 1 || s.n_kv_heads < 1 || s.head_dim < 16 || s.head_dim % 16 != 0 ||
-      s.page_size < 1 || s.diff_block != kDiffBlock || !(s.rope_theta > 1.0) ||
+      s.page_size < 1 || (s.diff_block != 16 && s.diff_block != kMaxDiffBlock) || !(s.rope_theta > 1.0) ||
       !std::isfinite(s.rope_theta))
     return TD_ERR_INVALID_ARG;
   const int64_t E = static_cast<int64_t>(s.n_kv_heads) * s.head_dim;
@@ -393,7 +395,7 @@ td_status td_pick_master(td_ctx* c, const td_round* r, const int32_t* sel, int32
   td_status s = prepare_round(c, r, st);
   if (s != TD_OK) return s;
   if (k > c->S) return TD_ERR_INVALID_ARG;
-  cudaError_t e = launch_pick_master(sel, c->N, c->S, k, cost_out, master_dev, c->d_pm_mask,
+  cudaError_t e = launch_pick_master(sel, c->N, c->S, c->shape.diff_block, k, cost_out, master_dev, c->d_pm_mask,
                                      c->d_ints + 5, c->d_err, st);
   if (e != cudaSuccess) return TD_ERR_CUDA;
   if (master_host) {
@@ -497,9 +499,9 @@ td_status td_diff_encode(td_ctx* c, const td_round* r, const int32_t* master,
   sc.agent_prefix = c->d_aprefix;
   sc.flag = c->d_flag;
   sc.row_count = reinterpret_cast<int32_t*>(
-      c->d_flag + static_cast<size_t>(c->N) * nl * ((c->S + kDiffBlock - 1) / kDiffBlock));
+      c->d_flag + static_cast<size_t>(c->N) * nl * round_dev(c).nb);
   sc.need_fixup = c->d_ints;
-  sc.nbw = (((c->S + kDiffBlock - 1) / kDiffBlock) + 31) / 32;
+  sc.nbw = (round_dev(c).nb + 31) / 32;
   cudaError_t e = launch_encode(c->g, round_dev(c), master,
                                 static_cast<const uint16_t*>(k_canon),
                                 static_cast<const uint16_t*>(v_canon), sel, k,

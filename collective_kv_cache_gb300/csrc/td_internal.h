@@ -15,7 +15,9 @@
 
 namespace td {
 
-constexpr int kDiffBlock = 16;     // tokens per diff block (canonical axis)
+constexpr int kTile = 16;          // canonical tokens per tile of the tile kernels
+constexpr int kDiffBlock = 16;     // default tokens per diff block (canonical axis)
+constexpr int kMaxDiffBlock = 32;  // diff blocks of 16 or 32 tokens (a 32-bit token mask)
 constexpr int kMaxListAgents = 256; // agents per restore launch (passed by value)
 
 TD_HD inline uint32_t err_bit(td_status s) { return 1u << static_cast<uint32_t>(s); }
@@ -29,7 +31,10 @@ struct Geom {
 
 // The current round's device tables (owned by the context).
 struct RoundDev {
-  int N, M, S, nb;
+  int N, M, S;
+  int B;                     // tokens per diff block (16 or 32, a multiple of kTile)
+  int nb;                    // diff blocks, ceil(S / B)
+  int nt;                    // tiles, ceil(S / kTile)
   const int32_t* off;        // [N*M] block start in each agent's prompt
   const float* cos_t;        // [N*M][D/2] cos of off * theta^(-2f/D), rounded to float
   const float* sin_t;        // [N*M][D/2]
@@ -99,7 +104,7 @@ cudaError_t launch_check_select(const Geom& g, const RoundDev& rd, const PoolDev
                                 int32_t* sel, uint32_t* err, cudaStream_t st);
 
 // gmask: [N][nbw] scratch; done: a counter that is zero between calls.
-cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int k, int64_t* cost,
+cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int B, int k, int64_t* cost,
                                int32_t* master, uint32_t* gmask, int* done, uint32_t* err,
                                cudaStream_t st);
 

@@ -161,7 +161,9 @@ extern "C" td_status td_check_select_noalloc(const td_shape* shape, const td_rou
   rd.N = N;
   rd.M = M;
   rd.S = static_cast<int>(S);
+  rd.B = kDiffBlock;
   rd.nb = static_cast<int>((S + kDiffBlock - 1) / kDiffBlock);
+  rd.nt = static_cast<int>((S + kTile - 1) / kTile);
   rd.off = reinterpret_cast<const int32_t*>(base + kOffOff);
   rd.cos_t = nullptr;  // the deviation pass turns nothing
   rd.sin_t = nullptr;

@@ -38,7 +38,8 @@ def _mini(**kw):
     return synth.RoundConfig(**base)
 
 
-CASES = {"tiny": synth.tiny(), "mini": _mini(), "qwen7b_3layers": synth.qwen7b().replace(n_layers=3)}
+CASES = {"tiny": synth.tiny(), "mini": _mini(), "mini_b32": _mini(diff_block=32, page_size=32),
+         "qwen7b_3layers": synth.qwen7b().replace(n_layers=3)}
 
 
 def _runner(cfg, rnd):

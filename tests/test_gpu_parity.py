@@ -4,8 +4,9 @@ Every stage is compared: the paged pool after re-rotation (including rows that m
 untouched), the deviations and selections, the master and its costs, the Master's dense
 cache, the CSR rows, block indices, diff values and slot map, and the pool after restore
 in both frames. Configurations span several tiles, ragged tails (shared spans not a
-multiple of 16, blocks that cross diff-block boundaries), page sizes 16, 24 and 32 and
-head layouts of 2x64, 4x128 and 8x128.
+multiple of 16, blocks that cross diff-block boundaries), page sizes 16, 24 and 32, diff
+blocks of 16 and 32 tokens (with a tile that lies wholly in a block's zero tail) and head
+layouts of 2x64, 4x128 and 8x128.
 """
 from __future__ import annotations
 
@@ -49,6 +50,16 @@ CASES = {
     "scale64_2layers": synth.scale64().replace(n_layers=2),
     "density40_p32_8agents_2layers": synth.density(40, page_size=32, pool_bytes=None).replace(
         n_agents=8, n_layers=2),
+    # diff block = page size (32 tokens), and 32-token blocks on 16-token pages
+    "mini_b32_p32": _mini(diff_block=32, page_size=32, seed=84),
+    "mini_b32_p16": _mini(diff_block=32, seed=85),
+    "mini_b32_pct100": _mini(diff_block=32, page_size=32, recompute_pct=100, seed=86),
+    "mini_b32_pad_tile": _mini(diff_block=32, page_size=32, block_lens=(20, 37, 16, 1), seed=87),
+    "mini_b32_uniform_scatter": _mini(diff_block=32, page_size=32, perturb_mode="uniform",
+                                      seed=88),
+    "qwen7b_b32_p32_3layers": synth.qwen7b().replace(n_layers=3, diff_block=32, page_size=32),
+    "density40_b32_p32_8agents_2layers": synth.density(40, page_size=32, pool_bytes=None).replace(
+        n_agents=8, n_layers=2, diff_block=32),
 }
 
 

@@ -271,7 +271,7 @@ def pin_k_rounding(orc):
 def pin_master(orc):
     rng = np.random.default_rng(21)
     for trial in range(60):
-        N, S, B = int(rng.integers(1, 7)), int(rng.integers(1, 200)), 16
+        N, S, B = int(rng.integers(1, 7)), int(rng.integers(1, 200)), int(rng.choice([16, 32]))
         k = int(rng.integers(0, S + 1))
         k = min(k, 12)
         sel = np.stack([np.sort(rng.choice(S, k, replace=False)) for _ in range(N)]).astype(np.int32)
@@ -348,8 +348,13 @@ def _canonical_agent_cache(orc, ch, i, l):
 
 def pin_roundtrip(orc):
     """restore(encode(X)) == X bitwise in the canonical frame, every agent and layer;
-    in the agent frame untouched tokens come back exactly as the rerotation wrote them."""
-    cfg = _mini_cfg()
+    in the agent frame untouched tokens come back exactly as the rerotation wrote them.
+    Diff blocks of 16 tokens, and of 32 tokens with 32-token pages (diff block = page)."""
+    for cfg in (_mini_cfg(), _mini_cfg(diff_block=32, page_size=32)):
+        _roundtrip(orc, cfg)
+
+
+def _roundtrip(orc, cfg):
     ch = rk.run_oracle_chain(rk.make_inputs(cfg, orc=orc), orc=orc, frame=1)
     N, L, S, B = cfg.n_agents, cfg.n_layers, cfg.n_shared, cfg.diff_block
     st = ch.store
