@@ -43,7 +43,7 @@ def _mix(z: np.ndarray) -> np.ndarray:
 
 def _tag(s) -> int:
     if isinstance(s, str):
-        h = 1469598103934665603  # FNV-1a over the tag's bytes
+        h = 1469598103934665603  # multiplicative byte hash of the tag (FNV's prime)
         for ch in s.encode():
             h = ((h ^ ch) * 1099511628211) & 0xFFFFFFFFFFFFFFFF
         return h
@@ -131,6 +131,41 @@ def noise_rows_torch(seed, tag, agent, layer, tokens, perturbed_rows, E):
                              0.5).reshape(-1, E)
         out[perturbed_rows] += big
     return out.to(torch.float32)
+
+
+def history_rows(cfg: "RoundConfig", agent: int, layer: int, kv: str, n: int,
+                 seed=None) -> np.ndarray:
+    """K or V of an agent's first n private-history positions at one layer, [n][E] bf16
+    bits, N(0, 1) (as stored in the pool: K already in the agent frame)."""
+    seed = cfg.seed if seed is None else seed
+    ctr = np.arange(n * cfg.elems, dtype=np.int64)
+    x = normal_f64(stream_key(seed, "hist", kv, agent, layer), ctr).astype(np.float32)
+    return f32_to_bf16_bits(x).reshape(n, cfg.elems)
+
+
+def history_torch(cfg: "RoundConfig", agent: int, layer: int, kv: str, n: int, device,
+                  seed=None):
+    """history_rows on `device`, [n][E] bf16 (same bits)."""
+    import torch
+    seed = cfg.seed if seed is None else seed
+    ctr = torch.arange(n * cfg.elems, dtype=torch.int64, device=device)
+    x = normal_torch(stream_key(seed, "hist", kv, agent, layer), ctr)
+    return x.to(torch.bfloat16).reshape(n, cfg.elems)
+
+
+def decode_queries(cfg: "RoundConfig", n_q_heads: int, agents, layer_begin: int, layer_end: int,
+                   seed=None) -> np.ndarray:
+    """One decode query per (layer, agent, query head), agent frame, N(0, 1):
+    [nl][len(agents)][n_q_heads][D] bf16 bits."""
+    seed = cfg.seed if seed is None else seed
+    D = cfg.head_dim
+    out = np.empty((layer_end - layer_begin, len(agents), n_q_heads, D), dtype=np.uint16)
+    ctr = np.arange(n_q_heads * D, dtype=np.int64)
+    for li in range(layer_end - layer_begin):
+        for x, a in enumerate(agents):
+            q = normal_f64(stream_key(seed, "query", int(a), layer_begin + li), ctr)
+            out[li, x] = f32_to_bf16_bits(q.astype(np.float32)).reshape(n_q_heads, D)
+    return out
 
 
 def randint(key, counters, lo: int, hi: int) -> np.ndarray:

@@ -267,6 +267,33 @@ class Oracle:
             _p(np.ascontiguousarray(vk), C.c_uint16), _p(np.ascontiguousarray(vv), C.c_uint16),
             _p(ag, C.c_int32), len(ag), layer_begin, layer_end, frame, C.byref(pl))
 
+    def attention(self, cfg, rnd_desc, master, store, agents, pool_arr, num_pages, block_table,
+                  q, n_q_heads, scale, layer_begin=0, layer_end=None):
+        """Decode attention from the Master and the diffs; q: uint16 bf16 bits
+        [nl][n_list][n_q_heads][D]. Returns (status, out float64, lse float64)."""
+        layer_end = cfg.n_layers if layer_end is None else layer_end
+        sh = self.shape(cfg)
+        rd = self.round_(*rnd_desc)
+        pl = self.pool(pool_arr, num_pages, block_table)
+        ag = np.ascontiguousarray(agents, dtype=np.int32)
+        nl, D = layer_end - layer_begin, cfg.head_dim
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        assert q.shape == (nl, len(ag), n_q_heads, D), q.shape
+        out = np.zeros((nl, len(ag), n_q_heads, D), dtype=np.float64)
+        lse = np.zeros((nl, len(ag), n_q_heads), dtype=np.float64)
+        vk = store["val_k"] if store["nnz"] else np.zeros((1, cfg.diff_block, cfg.elems), np.uint16)
+        vv = store["val_v"] if store["nnz"] else np.zeros((1, cfg.diff_block, cfg.elems), np.uint16)
+        ix = store["idx"] if store["nnz"] else np.zeros(1, np.int32)
+        st = self.lib.orc_attention(
+            C.byref(sh), C.byref(rd), master, _p(store["master_k"], C.c_uint16),
+            _p(store["master_v"], C.c_uint16), _p(store["rowptr"], C.c_int64),
+            _p(np.ascontiguousarray(ix, dtype=np.int32), C.c_int32),
+            _p(np.ascontiguousarray(vk), C.c_uint16), _p(np.ascontiguousarray(vv), C.c_uint16),
+            C.byref(pl), _p(ag, C.c_int32), len(ag), layer_begin, layer_end,
+            _p(q, C.c_uint16), n_q_heads, C.c_double(scale), _p(out, C.c_double),
+            _p(lse, C.c_double))
+        return st, out, lse
+
     def round_ratio(self, cfg, nnz: int) -> float:
         return float(self.lib.orc_round_ratio(cfg.n_agents, cfg.n_layers, cfg.n_shared,
                                               cfg.elems, cfg.diff_block, nnz))

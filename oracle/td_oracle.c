@@ -520,6 +520,106 @@ int orc_fused_restore(const orc_shape* sh, const orc_round* rd, int master,
   return status;
 }
 
+/* ------------------------------------------------------------------ attention */
+/* Decode attention read straight from the Master and the diffs. [B] §4.4 "Fused Diff
+ * Restore": the diff is applied block by block on chip and attention runs right after, with
+ * no materialised cache; [R] §8 (open questions: the restore fused inside the attention
+ * tile) and §9 (a paired block-sparse KV diff kernel aligned with FlashAttention).
+ * READING: agent a's context is its private history, positions [0, h_a), whose K/V are read
+ * from the paged pool as stored, followed by the shared blocks at their offsets: the shared
+ * token t of block j at local index u sits at position off_aj + u with K = R(off_aj) X_a(t)
+ * and V = X_a(t), X_a being the agent's canonical-frame cache (the Master's rows with a's
+ * records over them). One query per (agent, query head), in the agent frame; query head g
+ * reads kv head g / (n_q_heads / H). out = sum_p softmax_p(scale * q.k_p) v_p and
+ * lse = log sum_p exp(scale * q.k_p). Everything in float64, the rotation of K exactly from
+ * the bf16 values. The store holds exactly the layers [layer_begin, layer_end). */
+int orc_attention(const orc_shape* sh, const orc_round* rd, int master,
+                  const uint16_t* master_k, const uint16_t* master_v,
+                  const int64_t* rowptr, const int32_t* block_idx,
+                  const uint16_t* val_k, const uint16_t* val_v, const orc_pool* pool,
+                  const int32_t* agents, int n_list, int layer_begin, int layer_end,
+                  const uint16_t* q, int n_q_heads, double scale, double* out, double* lse) {
+  int N = rd->n_agents, M = rd->n_blocks, B = sh->diff_block, H = sh->n_kv_heads;
+  int D = sh->head_dim, P = sh->page_size;
+  int64_t E = (int64_t)H * D;
+  int S = shared_len(rd);
+  int nl = layer_end - layer_begin;
+  int nb = (S + B - 1) / B;
+  if (master < 0 || master >= N || n_q_heads < H || n_q_heads % H != 0 || nl < 0)
+    return ORC_ERR_ARG;
+  int G = n_q_heads / H;
+  int hmax = 0;
+  for (int i = 0; i < N; ++i) hmax = rd->hist_len[i] > hmax ? rd->hist_len[i] : hmax;
+  int64_t cap = (int64_t)hmax + S;
+  int32_t* off = malloc(sizeof(int32_t) * N * M);
+  int64_t* start = malloc(sizeof(int64_t) * (M + 1));
+  int32_t* tok_block = malloc(sizeof(int32_t) * (S + 1));
+  int64_t* row_of_block = malloc(sizeof(int64_t) * (nb > 0 ? nb : 1));
+  double* kx = malloc(sizeof(double) * (cap > 0 ? cap : 1) * E);   /* the context's K */
+  double* vx = malloc(sizeof(double) * (cap > 0 ? cap : 1) * E);   /* and V */
+  double* sc = malloc(sizeof(double) * (cap > 0 ? cap : 1));
+  int status = orc_offsets(rd, off);
+  canon_layout(rd, start, tok_block);
+  for (int li = 0; li < nl && status == ORC_OK; ++li) {
+    int l = layer_begin + li;
+    for (int x = 0; x < n_list && status == ORC_OK; ++x) {
+      int a = agents[x];
+      if (a < 0 || a >= N) { status = ORC_ERR_ARG; break; }
+      int64_t h = rd->hist_len[a], n = h + S;
+      /* the private history, as the pool holds it */
+      for (int64_t p = 0; p < h && status == ORC_OK; ++p) {
+        int64_t lp = p / P;
+        int32_t page = lp < pool->max_lp ? pool->block_table[(int64_t)a * pool->max_lp + lp] : -1;
+        if (page < 0 || page >= pool->num_pages) { status = ORC_ERR_UNMAPPED; break; }
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint16_t* src = pool->base +
+              ((((int64_t)l * 2 + kv) * pool->num_pages + page) * P + p % P) * E;
+          double* dst = (kv == 0 ? kx : vx) + p * E;
+          for (int64_t e = 0; e < E; ++e) dst[e] = (double)orc_bf16_to_f32(src[e]);
+        }
+      }
+      /* the shared blocks: the agent's canonical cache, K turned to the agent's offsets */
+      for (int b = 0; b < nb; ++b) row_of_block[b] = -1;
+      if (a != master) {
+        int64_t r0 = rowptr[(int64_t)a * nl + li], r1 = rowptr[(int64_t)a * nl + li + 1];
+        for (int64_t r = r0; r < r1; ++r) row_of_block[block_idx[r]] = r;
+      }
+      for (int64_t t = 0; t < S; ++t) {
+        int j = tok_block[t];
+        int64_t r = row_of_block[t / B];
+        const uint16_t* sk = r >= 0 ? val_k + (r * B + t % B) * E : master_k + ((int64_t)li * S + t) * E;
+        const uint16_t* sv = r >= 0 ? val_v + (r * B + t % B) * E : master_v + ((int64_t)li * S + t) * E;
+        orc_rotate_row_f64(sk, kx + (h + t) * E, H, D, off[(int64_t)a * M + j], sh->rope_theta, 0);
+        for (int64_t e = 0; e < E; ++e) vx[(h + t) * E + e] = (double)orc_bf16_to_f32(sv[e]);
+      }
+      /* softmax attention of every query head over the n context positions */
+      for (int g = 0; g < n_q_heads; ++g) {
+        int hk = g / G;
+        const uint16_t* qg = q + (((int64_t)li * n_list + x) * n_q_heads + g) * D;
+        double* og = out + (((int64_t)li * n_list + x) * n_q_heads + g) * D;
+        double mx = -INFINITY;
+        for (int64_t p = 0; p < n; ++p) {
+          double d = 0.0;
+          for (int e = 0; e < D; ++e)
+            d += (double)orc_bf16_to_f32(qg[e]) * kx[p * E + (int64_t)hk * D + e];
+          sc[p] = scale * d;
+          if (sc[p] > mx) mx = sc[p];
+        }
+        double sum = 0.0;
+        for (int64_t p = 0; p < n; ++p) sum += exp(sc[p] - mx);
+        for (int e = 0; e < D; ++e) {
+          double acc = 0.0;
+          for (int64_t p = 0; p < n; ++p) acc += exp(sc[p] - mx) * vx[p * E + (int64_t)hk * D + e];
+          og[e] = n > 0 ? acc / sum : 0.0;
+        }
+        if (lse) lse[((int64_t)li * n_list + x) * n_q_heads + g] = n > 0 ? mx + log(sum) : -INFINITY;
+      }
+    }
+  }
+  free(off); free(start); free(tok_block); free(row_of_block); free(kx); free(vx); free(sc);
+  return status;
+}
+
 /* ------------------------------------------------------------------ compression */
 /* [R] §7a: compression ratio = dense KV size / (Master + diffs) size. Dense size of one
  * agent: L*S*E bf16 for K and again for V. A diff block costs its K and V values

@@ -60,13 +60,31 @@ class Chain:
     pool_after_restore: Optional[np.ndarray] = None
 
 
-def make_inputs(cfg: synth.RoundConfig, seed: Optional[int] = None, orc=None) -> Chain:
+def make_inputs(cfg: synth.RoundConfig, seed: Optional[int] = None, orc=None,
+                map_history: bool = False) -> Chain:
     orc = orc or _oracle.get()
-    rnd = synth.make_round(cfg, seed)
+    rnd = synth.make_round(cfg, seed, map_history=map_history)
     desc = (rnd.block_len, rnd.hist_len, rnd.perm)
     off = orc.offsets(*desc)
     kc, vc = synth.canonical_kv(cfg, seed)
     return Chain(cfg, rnd, desc, off, positions(off, rnd.block_len), kc, vc)
+
+
+def fill_history(cfg: synth.RoundConfig, rnd: synth.Round, pool: np.ndarray,
+                 seed: Optional[int] = None) -> None:
+    """Writes every agent's private-history K/V (synth.history_rows) into its pages."""
+    P = cfg.page_size
+    for i, h in enumerate(rnd.hist_len):
+        h = int(h)
+        if h == 0:
+            continue
+        pos = np.arange(h)
+        pages = rnd.block_table[i, pos // P]
+        assert (pages >= 0).all()
+        for l in range(cfg.n_layers):
+            for kv, name in ((0, "K"), (1, "V")):
+                rows = synth.history_rows(cfg, i, l, name, h, seed)
+                pool[l, kv, pages, pos % P] = rows.reshape(h, cfg.n_kv_heads, cfg.head_dim)
 
 
 def fresh_check(ch: Chain, pool: np.ndarray) -> np.ndarray:

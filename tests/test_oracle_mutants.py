@@ -58,6 +58,20 @@ MUTANTS = {
     "restore_wrong_direction": ("if (frame == 0) orc_rotate_row(sk, kd, H, D, c, s, 0);",
                                 "if (frame == 0) orc_rotate_row(sk, kd, H, D, c, s, 1);"),
     "restore_wrong_row_token": ("val_k + (r * B + t % B) * E", "val_k + (r * B) * E"),
+    # attention read from the store
+    "attn_drops_history": ("int64_t h = rd->hist_len[a], n = h + S;",
+                           "int64_t h = rd->hist_len[a], n = S;"),
+    "attn_ignores_records": ("int64_t r = row_of_block[t / B];\n        const uint16_t* sk = r >= 0 ? val_k + (r * B + t % B) * E : master_k",
+                             "int64_t r = -1;\n        const uint16_t* sk = r >= 0 ? val_k + (r * B + t % B) * E : master_k"),
+    "attn_rotation_inverse": ("sh->rope_theta, 0);\n        for (int64_t e = 0; e < E; ++e) vx",
+                              "sh->rope_theta, 1);\n        for (int64_t e = 0; e < E; ++e) vx"),
+    "attn_offset_of_first_block": ("off[(int64_t)a * M + j], sh->rope_theta, 0);",
+                                   "off[(int64_t)a * M], sh->rope_theta, 0);"),
+    "attn_gqa_modulo": ("int hk = g / G;", "int hk = g % H;"),
+    "attn_no_scale": ("sc[p] = scale * d;", "sc[p] = d;"),
+    "attn_lse_without_max": ("n > 0 ? mx + log(sum) : -INFINITY;", "n > 0 ? log(sum) : -INFINITY;"),
+    "attn_history_from_k_only": ("          double* dst = (kv == 0 ? kx : vx) + p * E;",
+                                 "          double* dst = kx + p * E;"),
     # compression
     "ratio_without_master": ("return (double)n_agents * dense / (dense + diff + ptrs);",
                              "return (double)n_agents * dense / (diff + ptrs);"),

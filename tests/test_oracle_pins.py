@@ -466,12 +466,111 @@ def pin_compression(orc):
         assert round(caches, 1) == row["round_caches"], (row, caches)
 
 
+# ---------------------------------------------------------------- attention from the store
+def _attention_case(orc, cfg, n_q_heads, seed=None):
+    """Oracle chain (encode), the agents' private histories in the pool, seeded queries,
+    and the oracle's attention read from the Master and the diffs."""
+    ch = rk.run_oracle_chain(rk.make_inputs(cfg, seed, orc=orc, map_history=True), orc=orc,
+                             restore=False)
+    rnd = ch.rnd
+    pool = oracle.new_pool(cfg, rnd.num_pages)
+    rk.fill_history(cfg, rnd, pool, seed)
+    agents = list(range(cfg.n_agents))
+    q = synth.decode_queries(cfg, n_q_heads, agents, 0, cfg.n_layers, seed)
+    scale = 1.0 / math.sqrt(cfg.head_dim)
+    st, out, lse = orc.attention(cfg, ch.desc, ch.master, ch.store, agents, pool,
+                                 rnd.num_pages, rnd.block_table, q, n_q_heads, scale)
+    assert st == 0, st
+    return ch, pool, agents, q, scale, out, lse
+
+
+def pin_attention_matches_sdpa(orc):
+    """Against torch's scaled_dot_product_attention (float64) on a context assembled from
+    other pinned pieces: the history rows as the pool holds them, each shared position's
+    canonical row from the canonical-frame restore, turned by the float64 rotation to the
+    offset of the block that holds it (Figure 1's layout)."""
+    torch = pytest.importorskip("torch")
+    cfg = _mini_cfg(n_kv_heads=2, hist_range=(3, 40), seed=93)
+    nq = 6
+    ch, pool, agents, q, scale, out, lse = _attention_case(orc, cfg, nq)
+    rnd, H, D, P, L = ch.rnd, cfg.n_kv_heads, cfg.head_dim, cfg.page_size, cfg.n_layers
+    pool_c = oracle.new_pool(cfg, rnd.num_pages)
+    assert orc.fused_restore(cfg, ch.desc, ch.master, ch.store, np.arange(cfg.n_agents), pool_c,
+                             rnd.num_pages, rnd.block_table, frame=1) == 0
+    for x, a in enumerate(agents):
+        h = int(rnd.hist_len[a])
+        n = h + cfg.n_shared
+        starts = ch.off[a]
+        for l in range(L):
+            K = np.empty((n, H * D))
+            V = np.empty((n, H * D))
+            for p in range(n):
+                page, slot = rnd.block_table[a, p // P], p % P
+                if p < h:
+                    K[p] = synth.bf16_bits_to_f32(pool[l, 0, page, slot].reshape(-1))
+                    V[p] = synth.bf16_bits_to_f32(pool[l, 1, page, slot].reshape(-1))
+                else:
+                    j = int(np.nonzero((starts <= p) & (p < starts + rnd.block_len))[0][0])
+                    K[p] = orc.rotate_row_f64(pool_c[l, 0, page, slot].reshape(-1), H, D,
+                                              int(starts[j]), cfg.rope_theta, 0)
+                    V[p] = synth.bf16_bits_to_f32(pool_c[l, 1, page, slot].reshape(-1))
+            qt = torch.from_numpy(synth.bf16_bits_to_f32(q[l, x]).astype(np.float64))[None, :, None, :]
+            kt = torch.from_numpy(K.reshape(n, H, D).transpose(1, 0, 2)).repeat_interleave(nq // H, 0)[None]
+            vt = torch.from_numpy(V.reshape(n, H, D).transpose(1, 0, 2)).repeat_interleave(nq // H, 0)[None]
+            ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+            assert np.allclose(out[l, x], ref[0, :, 0].numpy(), rtol=0, atol=1e-10), (a, l)
+            ref_lse = torch.logsumexp(scale * (qt @ kt.transpose(-1, -2)), dim=-1)
+            assert np.allclose(lse[l, x], ref_lse[0, :, 0].numpy(), rtol=0, atol=1e-10), (a, l)
+
+
+def pin_attention_single_token(orc):
+    """A context of one token at position 0 (no history, one shared token, no diffs):
+    the output is that token's V and the log-sum-exp its scaled score."""
+    cfg = _mini_cfg(n_agents=1, n_layers=1, block_lens=(1,), hist_range=(0, 0), recompute_pct=0,
+                    check_layer=0, seed=94)
+    ch, pool, agents, q, scale, out, lse = _attention_case(orc, cfg, 4)
+    k = synth.bf16_bits_to_f32(ch.kc[0, 0]).astype(np.float64).reshape(2, -1)
+    v = synth.bf16_bits_to_f32(ch.vc[0, 0]).astype(np.float64).reshape(2, -1)
+    qf = synth.bf16_bits_to_f32(q[0, 0]).astype(np.float64)
+    for g in range(4):
+        assert np.array_equal(out[0, 0, g], v[g // 2])
+        assert abs(lse[0, 0, g] - scale * float(qf[g] @ k[g // 2])) <= 1e-12
+
+
+def pin_attention_constant_values(orc):
+    """Whatever the scores, a context whose V rows all equal c_h in kv head h returns c_h
+    for every query head that reads head h (query head g reads head g // (n_q / H))."""
+    cfg = _mini_cfg(n_kv_heads=2, hist_range=(3, 40), seed=95)
+    nq, H, D = 6, 2, cfg.head_dim
+    ch = rk.run_oracle_chain(rk.make_inputs(cfg, orc=orc, map_history=True), orc=orc,
+                             restore=False)
+    rnd = ch.rnd
+    pool = oracle.new_pool(cfg, rnd.num_pages)
+    rk.fill_history(cfg, rnd, pool)
+    c = synth.f32_to_bf16_bits(np.array([[0.5] * D, [-1.25] * D], np.float32)).reshape(-1)
+    st = dict(ch.store)
+    st["master_v"] = np.broadcast_to(c, st["master_v"].shape).copy()
+    if st["nnz"]:
+        st["val_v"] = np.broadcast_to(c, st["val_v"].shape).copy()
+    for i, h in enumerate(rnd.hist_len):
+        pos = np.arange(int(h))
+        pool[:, 1, rnd.block_table[i, pos // cfg.page_size], pos % cfg.page_size] = c.reshape(H, D)
+    q = synth.decode_queries(cfg, nq, range(cfg.n_agents), 0, cfg.n_layers)
+    s, out, _ = orc.attention(cfg, ch.desc, ch.master, st, list(range(cfg.n_agents)), pool,
+                              rnd.num_pages, rnd.block_table, q, nq, 0.3)
+    assert s == 0
+    want = synth.bf16_bits_to_f32(c).astype(np.float64).reshape(H, D)
+    for g in range(nq):
+        assert np.allclose(out[:, :, g], want[g // (nq // H)], rtol=0, atol=1e-12), g
+
+
 PINS = [pin_bf16, pin_offsets, pin_rope_table, pin_rotation_units, pin_rotation_bound,
         pin_rotation_group, pin_rerotate_absolute, pin_deviation, pin_topk,
         pin_select_recovers_perturbed, pin_k_rounding, pin_master, pin_master_min_dev,
         pin_select_group, pin_roundtrip,
         pin_v_only_difference, pin_identical_agents, pin_empty_selection_and_capacity,
-        pin_compression]
+        pin_compression, pin_attention_matches_sdpa, pin_attention_single_token,
+        pin_attention_constant_values]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
