@@ -268,9 +268,10 @@ class Oracle:
             _p(ag, C.c_int32), len(ag), layer_begin, layer_end, frame, C.byref(pl))
 
     def attention(self, cfg, rnd_desc, master, store, agents, pool_arr, num_pages, block_table,
-                  q, n_q_heads, scale, layer_begin=0, layer_end=None):
-        """Decode attention from the Master and the diffs; q: uint16 bf16 bits
-        [nl][n_list][n_q_heads][D]. Returns (status, out float64, lse float64)."""
+                  q, n_q_heads, scale, layer_begin=0, layer_end=None, from_pool=False):
+        """Decode attention from the Master and the diffs (from_pool: every position from
+        the pages); q: uint16 bf16 bits [nl][n_list][n_q_heads][D].
+        Returns (status, out float64, lse float64)."""
         layer_end = cfg.n_layers if layer_end is None else layer_end
         sh = self.shape(cfg)
         rd = self.round_(*rnd_desc)
@@ -290,8 +291,8 @@ class Oracle:
             _p(np.ascontiguousarray(ix, dtype=np.int32), C.c_int32),
             _p(np.ascontiguousarray(vk), C.c_uint16), _p(np.ascontiguousarray(vv), C.c_uint16),
             C.byref(pl), _p(ag, C.c_int32), len(ag), layer_begin, layer_end,
-            _p(q, C.c_uint16), n_q_heads, C.c_double(scale), _p(out, C.c_double),
-            _p(lse, C.c_double))
+            _p(q, C.c_uint16), n_q_heads, C.c_double(scale), int(from_pool),
+            _p(out, C.c_double), _p(lse, C.c_double))
         return st, out, lse
 
     def round_ratio(self, cfg, nnz: int) -> float:

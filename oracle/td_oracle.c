@@ -532,13 +532,16 @@ int orc_fused_restore(const orc_shape* sh, const orc_round* rd, int master,
  * records over them). One query per (agent, query head), in the agent frame; query head g
  * reads kv head g / (n_q_heads / H). out = sum_p softmax_p(scale * q.k_p) v_p and
  * lse = log sum_p exp(scale * q.k_p). Everything in float64, the rotation of K exactly from
- * the bf16 values. The store holds exactly the layers [layer_begin, layer_end). */
+ * the bf16 values. The store holds exactly the layers [layer_begin, layer_end).
+ * from_pool != 0: the same attention with every position [0, h_a + S) read from the pages
+ * as stored (a restored cache); the store is not read. */
 int orc_attention(const orc_shape* sh, const orc_round* rd, int master,
                   const uint16_t* master_k, const uint16_t* master_v,
                   const int64_t* rowptr, const int32_t* block_idx,
                   const uint16_t* val_k, const uint16_t* val_v, const orc_pool* pool,
                   const int32_t* agents, int n_list, int layer_begin, int layer_end,
-                  const uint16_t* q, int n_q_heads, double scale, double* out, double* lse) {
+                  const uint16_t* q, int n_q_heads, double scale, int from_pool, double* out,
+                  double* lse) {
   int N = rd->n_agents, M = rd->n_blocks, B = sh->diff_block, H = sh->n_kv_heads;
   int D = sh->head_dim, P = sh->page_size;
   int64_t E = (int64_t)H * D;
@@ -565,7 +568,8 @@ int orc_attention(const orc_shape* sh, const orc_round* rd, int master,
     for (int x = 0; x < n_list && status == ORC_OK; ++x) {
       int a = agents[x];
       if (a < 0 || a >= N) { status = ORC_ERR_ARG; break; }
-      int64_t h = rd->hist_len[a], n = h + S;
+      int64_t n = (int64_t)rd->hist_len[a] + S;
+      int64_t h = from_pool ? n : rd->hist_len[a];   /* positions read from the pages */
       /* the private history, as the pool holds it */
       for (int64_t p = 0; p < h && status == ORC_OK; ++p) {
         int64_t lp = p / P;
@@ -580,11 +584,11 @@ int orc_attention(const orc_shape* sh, const orc_round* rd, int master,
       }
       /* the shared blocks: the agent's canonical cache, K turned to the agent's offsets */
       for (int b = 0; b < nb; ++b) row_of_block[b] = -1;
-      if (a != master) {
+      if (a != master && !from_pool) {
         int64_t r0 = rowptr[(int64_t)a * nl + li], r1 = rowptr[(int64_t)a * nl + li + 1];
         for (int64_t r = r0; r < r1; ++r) row_of_block[block_idx[r]] = r;
       }
-      for (int64_t t = 0; t < S; ++t) {
+      for (int64_t t = 0; t < S && !from_pool; ++t) {
         int j = tok_block[t];
         int64_t r = row_of_block[t / B];
         const uint16_t* sk = r >= 0 ? val_k + (r * B + t % B) * E : master_k + ((int64_t)li * S + t) * E;

@@ -130,13 +130,15 @@ int orc_fused_restore(const orc_shape* sh, const orc_round* rd, int master,
 /* Decode attention of the listed agents read straight from the Master and the diffs
  * (no restored cache): history K/V from the pool, shared K = R(off) X_a, V = X_a; float64.
  * q [nl][n_list][n_q_heads][D] bf16, out [nl][n_list][n_q_heads][D], lse [nl][n_list][n_q_heads]
- * or NULL. The store holds exactly the layers [layer_begin, layer_end). */
+ * or NULL. The store holds exactly the layers [layer_begin, layer_end). from_pool != 0:
+ * every position [0, h_a + S) from the pages instead (a restored cache). */
 int orc_attention(const orc_shape* sh, const orc_round* rd, int master,
                   const uint16_t* master_k, const uint16_t* master_v,
                   const int64_t* rowptr, const int32_t* block_idx,
                   const uint16_t* val_k, const uint16_t* val_v, const orc_pool* pool,
                   const int32_t* agents, int n_list, int layer_begin, int layer_end,
-                  const uint16_t* q, int n_q_heads, double scale, double* out, double* lse);
+                  const uint16_t* q, int n_q_heads, double scale, int from_pool, double* out,
+                  double* lse);
 
 /* Compression ratios (Performance Evaluation, metric "compression ratio"). */
 double orc_round_ratio(int n_agents, int n_layers, int n_shared, int elems, int diff_block,

@@ -59,8 +59,10 @@ MUTANTS = {
                                 "if (frame == 0) orc_rotate_row(sk, kd, H, D, c, s, 1);"),
     "restore_wrong_row_token": ("val_k + (r * B + t % B) * E", "val_k + (r * B) * E"),
     # attention read from the store
-    "attn_drops_history": ("int64_t h = rd->hist_len[a], n = h + S;",
-                           "int64_t h = rd->hist_len[a], n = S;"),
+    "attn_drops_history": ("int64_t n = (int64_t)rd->hist_len[a] + S;",
+                           "int64_t n = S;"),
+    "attn_pool_mode_reads_store": ("int64_t h = from_pool ? n : rd->hist_len[a];",
+                                   "int64_t h = rd->hist_len[a];"),
     "attn_ignores_records": ("int64_t r = row_of_block[t / B];\n        const uint16_t* sk = r >= 0 ? val_k + (r * B + t % B) * E : master_k",
                              "int64_t r = -1;\n        const uint16_t* sk = r >= 0 ? val_k + (r * B + t % B) * E : master_k"),
     "attn_rotation_inverse": ("sh->rope_theta, 0);\n        for (int64_t e = 0; e < E; ++e) vx",

@@ -521,6 +521,24 @@ def pin_attention_matches_sdpa(orc):
             assert np.allclose(out[l, x], ref[0, :, 0].numpy(), rtol=0, atol=1e-10), (a, l)
             ref_lse = torch.logsumexp(scale * (qt @ kt.transpose(-1, -2)), dim=-1)
             assert np.allclose(lse[l, x], ref_lse[0, :, 0].numpy(), rtol=0, atol=1e-10), (a, l)
+    # from the pages: the agent-frame restore (history kept) read as stored
+    assert orc.fused_restore(cfg, ch.desc, ch.master, ch.store, np.arange(cfg.n_agents), pool,
+                             rnd.num_pages, rnd.block_table, frame=0) == 0
+    q2 = synth.decode_queries(cfg, nq, agents, 0, L, seed=7)
+    st, out2, _ = orc.attention(cfg, ch.desc, ch.master, ch.store, agents, pool, rnd.num_pages,
+                                rnd.block_table, q2, nq, scale, from_pool=True)
+    assert st == 0
+    for x, a in enumerate(agents):
+        n = int(rnd.hist_len[a]) + cfg.n_shared
+        pos = np.arange(n)
+        for l in range(L):
+            K = synth.bf16_bits_to_f32(rk.gather_rows(pool, rnd.block_table, P, a, l, 0, pos)).astype(np.float64)
+            V = synth.bf16_bits_to_f32(rk.gather_rows(pool, rnd.block_table, P, a, l, 1, pos)).astype(np.float64)
+            qt = torch.from_numpy(synth.bf16_bits_to_f32(q2[l, x]).astype(np.float64))[None, :, None, :]
+            kt = torch.from_numpy(K.reshape(n, H, D).transpose(1, 0, 2)).repeat_interleave(nq // H, 0)[None]
+            vt = torch.from_numpy(V.reshape(n, H, D).transpose(1, 0, 2)).repeat_interleave(nq // H, 0)[None]
+            ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+            assert np.allclose(out2[l, x], ref[0, :, 0].numpy(), rtol=0, atol=1e-10), (a, l)
 
 
 def pin_attention_single_token(orc):
