@@ -27,7 +27,7 @@ CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", "-fno-fast-math"
              "-Wextra"]
 
 CU_SOURCES = ["k_rerotate.cu", "k_select.cu", "k_master.cu", "k_encode.cu", "k_restore.cu",
-              "k_variants.cu", "td_noalloc.cu"]
+              "k_variants.cu", "td_noalloc.cu", "k_attention.cu"]
 CXX_SOURCES = ["td_host.cpp", "td_rounds.cpp"]
 HEADERS = ["td_internal.h", "td_device.cuh"]
 

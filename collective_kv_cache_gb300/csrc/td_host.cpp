@@ -51,6 +51,8 @@ struct td_ctx {
                                     // pick_master's counter, spare
   int64_t* d_bound = nullptr;
   uint32_t* d_err = nullptr;
+  float* d_attn = nullptr;          // attention partials, grown on demand
+  size_t attn_cap = 0;              // its size in floats
   // pinned host words for results
   int64_t* h_words = nullptr;       // [4]
 };
@@ -87,6 +89,7 @@ void free_ctx(td_ctx* c) {
   cudaFree(c->d_ints);
   cudaFree(c->d_bound);
   cudaFree(c->d_err);
+  cudaFree(c->d_attn);
   if (c->h_stage) cudaFreeHost(c->h_stage);
   if (c->h_words) cudaFreeHost(c->h_words);
   if (c->stage_done) cudaEventDestroy(c->stage_done);
@@ -221,6 +224,104 @@ td_status pool_dev(const td_ctx* c, const td_round* r, const td_paged* p, PoolDe
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Decode attention of the listed agents: shared positions from the store (store != null)
+// or every position from the pages (store == null, the restored cache).
+td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store,
+                        const td_paged* pool, const int32_t* agents, int32_t n_list,
+                        int32_t layer_begin, int32_t layer_end, const void* q,
+                        int32_t n_q_heads, float scale, float* out, float* lse, void* stream) {
+  if (!c || !same_device(c) || n_list < 0 || (n_list > 0 && (!agents || !q || !out)))
+    return TD_ERR_INVALID_ARG;
+  const int H = c->g.H, D = c->g.D;
+  if ((D != 64 && D != 128) || n_q_heads < H || n_q_heads % H != 0 ||
+      n_q_heads / H > kAttnGMax || !std::isfinite(scale))
+    return TD_ERR_INVALID_ARG;
+  if (layer_begin < 0 || layer_end > c->shape.n_layers || layer_begin >= layer_end)
+    return TD_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) & 3u) != 0) return TD_ERR_INVALID_ARG;
+  if (store) {
+    if (!store->master_k || !store->master_v || !store->slot || !aligned16(store->master_k) ||
+        !aligned16(store->master_v) || (store->val_k && !aligned16(store->val_k)) ||
+        (store->val_v && !aligned16(store->val_v)))
+      return TD_ERR_INVALID_ARG;
+    if (layer_begin < store->layer_begin || layer_end > store->layer_end ||
+        store->layer_begin < 0 || store->layer_end > c->shape.n_layers)
+      return TD_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  td_status s = prepare_round(c, r, st);
+  if (s != TD_OK) return s;
+  for (int x = 0; x < n_list; ++x)
+    if (agents[x] < 0 || agents[x] >= c->N) return TD_ERR_INVALID_ARG;
+  if (n_list == 0) return TD_OK;
+  PoolDev pd;
+  if ((s = pool_dev(c, r, pool, &pd)) != TD_OK) return s;
+  AttnArgs a{};
+  a.g = c->g;
+  a.rd = round_dev(c);
+  a.pool = pd;
+  if (store) {
+    a.store.master_k = static_cast<uint16_t*>(store->master_k);
+    a.store.master_v = static_cast<uint16_t*>(store->master_v);
+    a.store.rowptr = store->rowptr;
+    a.store.block_idx = store->block_idx;
+    a.store.val_k = static_cast<uint16_t*>(store->val_k);
+    a.store.val_v = static_cast<uint16_t*>(store->val_v);
+    a.store.slot = store->slot;
+    a.store.capacity = store->capacity_blocks;
+    a.store.nl = store->layer_end - store->layer_begin;
+    a.sl0 = layer_begin - store->layer_begin;
+  }
+  a.q = static_cast<const uint16_t*>(q);
+  a.out = out;
+  a.lse = lse;
+  a.n_list = n_list;
+  a.nq = n_q_heads;
+  a.G = n_q_heads / H;
+  a.nl = layer_end - layer_begin;
+  a.layer_begin = layer_begin;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = c->d_err;
+  // partials of the largest launch; grown once, after the work that used them
+  auto units_of = [&](int x) {
+    return (static_cast<int64_t>(r->hist_len[agents[x]]) + c->S + kAttnChunk - 1) / kAttnChunk;
+  };
+  int64_t most = 0;
+  for (int x0 = 0; x0 < n_list; x0 += kMaxListAgents) {
+    int64_t sum = 0;
+    for (int x = x0; x < n_list && x < x0 + kMaxListAgents; ++x) sum += units_of(x);
+    most = sum > most ? sum : most;
+  }
+  const size_t need = static_cast<size_t>(most) * a.nl * H * kAttnGMax * (D + 2);
+  if (need > c->attn_cap) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TD_ERR_CUDA;
+    cudaFree(c->d_attn);
+    c->d_attn = nullptr;
+    c->attn_cap = 0;
+    if (cudaMalloc(&c->d_attn, need * sizeof(float)) != cudaSuccess) return TD_ERR_CUDA;
+    c->attn_cap = need;
+  }
+  for (int x0 = 0; x0 < n_list; x0 += kMaxListAgents) {
+    AttnList L;
+    L.n = n_list - x0 < kMaxListAgents ? n_list - x0 : kMaxListAgents;
+    L.base[0] = 0;
+    for (int x = 0; x < L.n; ++x) {
+      L.a[x] = agents[x0 + x];
+      L.hist[x] = r->hist_len[agents[x0 + x]];
+      const int64_t nb = L.base[x] + units_of(x0 + x);
+      if (nb > INT32_MAX) return TD_ERR_INVALID_ARG;
+      L.base[x + 1] = static_cast<int32_t>(nb);
+    }
+    const int64_t units = static_cast<int64_t>(L.base[L.n]) * a.nl * H;
+    if (units > INT32_MAX) return TD_ERR_INVALID_ARG;
+    a.x0 = x0;
+    a.part_o = c->d_attn;
+    a.part_ml = c->d_attn + static_cast<size_t>(units) * kAttnGMax * D;
+    if (launch_attention(a, L, store == nullptr, st) != cudaSuccess) return TD_ERR_CUDA;
+  }
+  return TD_OK;
+}
 
 }  // namespace
 
@@ -602,6 +703,24 @@ td_status td_materialise_mirror(td_ctx* c, const td_round* r, const td_diff_stor
                          static_cast<uint16_t*>(dense_v), c->d_err, st) != cudaSuccess)
     return TD_ERR_CUDA;
   return TD_OK;
+}
+
+td_status td_fused_attention(td_ctx* c, const td_round* r, const td_diff_store* store,
+                             const td_paged* pool, const int32_t* agents, int32_t n_list,
+                             int32_t layer_begin, int32_t layer_end, const void* q,
+                             int32_t n_q_heads, float scale, float* out, float* lse,
+                             void* stream) {
+  if (!store) return TD_ERR_INVALID_ARG;
+  return run_attention(c, r, store, pool, agents, n_list, layer_begin, layer_end, q, n_q_heads,
+                       scale, out, lse, stream);
+}
+
+td_status td_paged_attention(td_ctx* c, const td_round* r, const td_paged* pool,
+                             const int32_t* agents, int32_t n_list, int32_t layer_begin,
+                             int32_t layer_end, const void* q, int32_t n_q_heads, float scale,
+                             float* out, float* lse, void* stream) {
+  return run_attention(c, r, nullptr, pool, agents, n_list, layer_begin, layer_end, q, n_q_heads,
+                       scale, out, lse, stream);
 }
 
 td_status td_get_error(td_ctx* c, void* stream, uint32_t* bits_out) {

@@ -128,6 +128,39 @@ cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& poo
                            int store_layer0, int nl, int frame, uint32_t* err,
                            cudaStream_t st);
 
+// Decode attention from the Master and the diffs (k_attention.cu).
+constexpr int kAttnChunk = 512;    // context positions per work unit (one warp)
+constexpr int kAttnStage = 16;     // positions per pipeline stage
+constexpr int kAttnDepth = 3;      // stages in flight per unit
+constexpr int kAttnGMax = 8;       // query heads per kv head
+
+struct AttnList {
+  int n;                               // agents of this launch
+  int32_t a[kMaxListAgents];           // their ids
+  int32_t hist[kMaxListAgents];        // their history lengths
+  int32_t base[kMaxListAgents + 1];    // exclusive prefix of their units (per layer, head)
+};
+
+struct AttnArgs {
+  Geom g;
+  RoundDev rd;
+  PoolDev pool;
+  StoreDev store;            // unused when every position comes from the pages
+  const uint16_t* q;         // [nl][n_list][nq][D] bf16
+  float* out;                // [nl][n_list][nq][D]
+  float* lse;                // [nl][n_list][nq] or nullptr
+  float* part_o;             // [units][kAttnGMax][D]
+  float* part_ml;            // [units][kAttnGMax][2]: max, sum (base 2)
+  int n_list, x0;            // the whole list's length; this launch's first entry
+  int nq, G;                 // query heads, query heads per kv head
+  int nl, layer_begin, sl0;  // layers; store layer of layer_begin
+  float scale_log2;          // softmax scale * log2(e)
+  uint32_t* err;
+};
+
+cudaError_t launch_attention(const AttnArgs& a, const AttnList& list, bool from_pool,
+                             cudaStream_t st);
+
 cudaError_t launch_materialise(const Geom& g, const RoundDev& rd, const StoreDev& store,
                                int agent, int sl0, int nl, uint16_t* dk, uint16_t* dv,
                                uint32_t* err, cudaStream_t st);

@@ -89,6 +89,10 @@ def _load() -> C.CDLL:
                                   P(I32), VP],
         "td_pick_master_min_deviation": [VP, P(td_round), VP, I32, VP, VP, VP, P(I32), VP],
         "td_materialise_mirror": [VP, P(td_round), P(td_diff_store), I32, I32, I32, VP, VP, VP],
+        "td_fused_attention": [VP, P(td_round), P(td_diff_store), P(td_paged), VP, I32, I32, I32,
+                               VP, I32, C.c_float, VP, VP, VP],
+        "td_paged_attention": [VP, P(td_round), P(td_paged), VP, I32, I32, I32, VP, I32,
+                               C.c_float, VP, VP, VP],
         "td_form_rounds": [P(td_prompt), I32, I32, I32, VP, I32, VP, VP, P(I32)],
         "td_group_round": [P(td_prompt), I32, I32, VP, I32, I32, I32, VP, P(I32), VP, P(I32),
                            VP, VP],
@@ -109,7 +113,8 @@ EXPORTS = ("td_ctx_create", "td_ctx_destroy", "td_status_string", "td_round_offs
            "td_rerotate_batched", "td_check_select", "td_pick_master", "td_diff_encode",
            "td_fused_restore", "td_get_error", "td_check_select_noalloc",
            "td_check_select_group", "td_pick_master_min_deviation", "td_segment_hash",
-           "td_form_rounds", "td_group_round", "td_materialise_mirror")
+           "td_form_rounds", "td_group_round", "td_materialise_mirror",
+           "td_fused_attention", "td_paged_attention")
 
 
 def lib_path() -> str:
@@ -215,6 +220,24 @@ def td_pick_master_min_deviation(ctx, rnd, sel, k, dev, score_out, master_dev, s
         _check(s, "td_pick_master_min_deviation")
         return m.value
     return s, m.value
+
+
+def td_fused_attention(ctx, rnd, store, pool, agents, layer_begin, layer_end, q, n_q_heads,
+                       scale, out, lse=None, stream=0, check=True) -> int:
+    ag = np.ascontiguousarray(agents, dtype=np.int32)
+    s = _lib.td_fused_attention(ctx, C.byref(rnd), C.byref(store), C.byref(pool),
+                                ag.ctypes.data if ag.size else None, ag.size, layer_begin,
+                                layer_end, q, n_q_heads, scale, out, lse, stream)
+    return _check(s, "td_fused_attention") if check else s
+
+
+def td_paged_attention(ctx, rnd, pool, agents, layer_begin, layer_end, q, n_q_heads, scale, out,
+                       lse=None, stream=0, check=True) -> int:
+    ag = np.ascontiguousarray(agents, dtype=np.int32)
+    s = _lib.td_paged_attention(ctx, C.byref(rnd), C.byref(pool),
+                                ag.ctypes.data if ag.size else None, ag.size, layer_begin,
+                                layer_end, q, n_q_heads, scale, out, lse, stream)
+    return _check(s, "td_paged_attention") if check else s
 
 
 def td_materialise_mirror(ctx, rnd, store, agent, layer_begin, layer_end, dense_k, dense_v,

@@ -263,6 +263,46 @@ td_status td_check_select_noalloc(const td_shape* shape, const td_round* round,
                                   const void* k_fresh, int32_t recompute_pct, int32_t* sel,
                                   int32_t* k_out, uint32_t* err_bits_out, void* stream);
 
+/* Decode attention read straight from the Master and the diffs: the restore fused into
+ * attention ([B] §4.4 "Fused Diff Restore": diffs applied block by block on chip, attention
+ * right after, no materialised cache; [R] §8 open questions and §9). For every listed agent
+ * a, layer l in [layer_begin, layer_end) and query head g: the context is a's private
+ * history (positions [0, h_a), K/V read from the pages as stored; those pages must be
+ * mapped) and its shared tokens (the Master's rows with a's records over them, in the
+ * canonical frame): the shared token of block j at local index u has position off_aj + u,
+ * K = R(off_aj) X and V = X. The pages of the shared span are not read.
+ *   out[l][x][g] = sum_p softmax_p(scale * q[l][x][g] . K_p) V_p over the context
+ *   lse[l][x][g] = ln sum_p exp(scale * q[l][x][g] . K_p)
+ * Query head g reads kv head g / (n_q_heads / H) (grouped queries, at most 8 per kv head).
+ * The kernel turns the query by R(-off_aj) once per block instead of turning keys.
+ * Arithmetic: scores in float32 (a turned query split into two bf16 parts on the tensor
+ * cores: 16 bits of the query kept), softmax and the weighted sum of V in float32.
+ *   store     the round's Master-Mirror store; [layer_begin, layer_end) within its layers
+ *   pool      the agents' pages (history), as for td_fused_restore
+ *   agents    HOST [n_list] agent indices
+ *   q         DEVICE bf16 [layer_end-layer_begin][n_list][n_q_heads][D], agent frame (rotated
+ *             at the query's position), 4-byte aligned
+ *   out       DEVICE float [layer_end-layer_begin][n_list][n_q_heads][D]
+ *   lse       DEVICE float [layer_end-layer_begin][n_list][n_q_heads], or NULL
+ * Head dims 64 and 128 (else TD_ERR_INVALID_ARG). The context owns the partial results'
+ * scratch and grows it when a call needs more (synchronising the stream first). An
+ * unmapped history page sets TD_ERR_UNMAPPED_PAGE in the error word; a bounded wait on the
+ * copy engine that runs out sets TD_ERR_DEVICE_TIMEOUT (that unit's result is not written). */
+td_status td_fused_attention(td_ctx* ctx, const td_round* round, const td_diff_store* store,
+                             const td_paged* pool, const int32_t* agents, int32_t n_list,
+                             int32_t layer_begin, int32_t layer_end, const void* q,
+                             int32_t n_q_heads, float scale, float* out, float* lse,
+                             void* stream);
+
+/* Comparison baseline, not on the path: the same decode attention over a restored cache,
+ * every position [0, h_a + S) read from the agent's pages (after td_fused_restore, frame
+ * 0): the unfused "restore, then attend" the pages compare against. Arguments and
+ * arithmetic as td_fused_attention (queries used as given, no turning). */
+td_status td_paged_attention(td_ctx* ctx, const td_round* round, const td_paged* pool,
+                             const int32_t* agents, int32_t n_list, int32_t layer_begin,
+                             int32_t layer_end, const void* q, int32_t n_q_heads, float scale,
+                             float* out, float* lse, void* stream);
+
 /* Comparison baseline, not on the path: the dense restore that td_fused_restore replaces
  * ([R] §3d and Figure 5: materialise the Mirror, then copy it into pages). Writes agent's
  * canonical-frame cache X_agent for layers [layer_begin, layer_end): the Master's rows
