@@ -408,6 +408,7 @@ def bench_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device error word {bits:#x} in the timed region")
 
     comparisons = None if args.no_compare else compare_baselines(st, agents, stage_ms, device)
+    attention = None if args.no_attention else bench_attention(cfg, seed, device)
 
     by = stage_bytes(cfg, N, L, st["k"], st["nnz"], N)
     step_bytes = sum(by.values())
@@ -462,6 +463,7 @@ def bench_ours(args, rank, world, local_rank):
             "stages_sequential_ms": round(seq_ms, 5),
             "clocks": clk.summary(),
             "comparisons": comparisons,
+            "attention": attention,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -506,6 +508,100 @@ def compare_baselines(st, agents, stage_ms, device, reps=3):
             "fused_speedup": round(dense / stage_ms["restore"], 3),
             "what": "same round and kernels; serial = per-agent re-rotation + selection; "
                     "dense = materialise each agent's cache, then re-rotate it into pages"}
+
+
+def attention_bytes(cfg, hist, nnz, n_q_heads, from_pool: bool) -> int:
+    """Algorithmic bytes of one decode-attention call over all layers and agents: each
+    agent's history K/V (read from its pages); the shared span's K/V either from the store
+    (the Master once for all agents, plus each agent's records, whole blocks) or, over a
+    restored cache, from every agent's pages; the bf16 queries, float outputs and lse."""
+    L, S, E, B = cfg.n_layers, cfg.n_shared, cfg.elems, cfg.diff_block
+    N = len(hist)
+    by = int(sum(hist)) * L * E * 4
+    by += N * S * L * E * 4 if from_pool else S * L * E * 4 + nnz * B * E * 4
+    rows = L * N * n_q_heads
+    return by + rows * cfg.head_dim * (2 + 4) + rows * 4
+
+
+def bench_attention(cfg, seed, device, reps=10):
+    """Decode attention of every agent over its context, all layers, read straight from the
+    Master and the diffs (td_fused_attention), against the unfused path: restore every
+    agent's pages (td_fused_restore), then attend over them (td_paged_attention). Its own
+    round with the histories' pages mapped and filled; CUDA events on the launching stream,
+    mean of `reps` after warm-up; the working set is far above the L2."""
+    import math
+    import torch
+    from collective_kv_cache_gb300 import runner as R
+    from collective_kv_cache_gb300 import synth, td, workload
+    nq = cfg.n_q_heads or cfg.n_kv_heads
+    rnd = synth.make_round(cfg, seed, map_history=True)
+    rr = R.RoundRunner(cfg, rnd.block_len, rnd.hist_len, rnd.perm, rnd.block_table,
+                       rnd.num_pages, device=device)
+    kc, vc = workload.canonical(cfg, device, seed)
+    rr.rerotate(kc, vc)
+    kf = workload.fresh_check(rr, rnd, seed)
+    sel = rr.check_select(kf)
+    master = rr.pick_master()
+    sel_np = sel.cpu().numpy()
+    kfs, vfs = workload.fresh_selected(rr, rnd, sel_np, vc, seed)
+    rr.alloc_store(max(rr.candidate_bound(master), 1))
+    nnz = rr.diff_encode(kc, vc, kfs, vfs)
+    del kf, kfs, vfs
+    workload.fill_history(rr, rnd, seed)
+    N, L = cfg.n_agents, cfg.n_layers
+    agents = list(range(N))
+    q = R.to_device_bf16(synth.decode_queries(cfg, nq, agents, 0, L, seed), device)
+    scale = 1.0 / math.sqrt(cfg.head_dim)
+    out_f = torch.empty(q.shape, dtype=torch.float32, device=device)
+    out_p = torch.empty_like(out_f)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=device)
+
+    def fused():
+        td.td_fused_attention(rr.ctx.handle, rr.round, rr.store, rr.pool, agents, 0, L,
+                              q.data_ptr(), nq, scale, out_f.data_ptr(), lse.data_ptr(), rr.s)
+
+    def paged():
+        td.td_paged_attention(rr.ctx.handle, rr.round, rr.pool, agents, 0, L, q.data_ptr(), nq,
+                              scale, out_p.data_ptr(), lse.data_ptr(), rr.s)
+
+    def restore_then_paged():
+        rr.fused_restore(agents)
+        paged()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(rr.stream)
+        for _ in range(reps):
+            fn()
+        b.record(rr.stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    t_fused = timed(fused)
+    t_unfused = timed(restore_then_paged)
+    t_paged = timed(paged)
+    s, bits = rr.get_error()
+    if s != 0:
+        raise RuntimeError(f"device error word {bits:#x} in the attention comparison")
+    diff = float((out_f - out_p).abs().max().item())
+    by_f = attention_bytes(cfg, rnd.hist_len, nnz, nq, from_pool=False)
+    by_p = attention_bytes(cfg, rnd.hist_len, nnz, nq, from_pool=True)
+    by_r = stage_bytes(cfg, N, L, sel_np.shape[1], nnz, N)["restore"]
+    peak, peak_kind = measured_peak()
+    gbs = by_f / (t_fused * 1e-3) / 1e9
+    return {"fused_ms": round(t_fused, 5), "fused_bytes": by_f, "fused_gbs": round(gbs, 1),
+            "fused_frac": round(gbs / peak, 4), "peak": peak, "peak_kind": peak_kind,
+            "restore_then_paged_ms": round(t_unfused, 5),
+            "paged_ms": round(t_paged, 5), "paged_bytes": by_p,
+            "paged_gbs": round(by_p / (t_paged * 1e-3) / 1e9, 1),
+            "restore_bytes": by_r, "fused_speedup": round(t_unfused / t_fused, 3),
+            "query_heads": nq, "max_abs_diff_fused_vs_restored": diff,
+            "what": "decode attention of all agents over all layers (history + shared span); "
+                    "fused = from the Master and the diffs; unfused = restore all agents' "
+                    "pages, then paged attention"}
 
 
 def report_chunked(args, cfg, seed, device, rank, world):
@@ -768,6 +864,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the serial-PIC and dense-restore comparison baselines")
+    ap.add_argument("--no-attention", action="store_true",
+                    help="skip the fused-attention measurement")
     ap.add_argument("--cpu-layers", type=int, default=None)
     ap.add_argument("--ref-layers", type=int, default=4)
     args = ap.parse_args(argv)

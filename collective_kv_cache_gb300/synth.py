@@ -210,6 +210,7 @@ class RoundConfig:
     diff_block: int = 16
     pool_bytes: Optional[int] = None  # paged pool size; None = exactly the pages needed
     seed: int = 1000
+    n_q_heads: int = 0                # decode query heads (0: as many as kv heads)
 
     @property
     def n_blocks(self) -> int:
@@ -243,21 +244,21 @@ def qwen7b() -> RoundConfig:
     return RoundConfig(
         name="qwen2.5-7b_n10_l28_h4x128_s2560", n_agents=10, n_layers=28, n_kv_heads=4,
         head_dim=128, page_size=16, block_lens=(256,) * 10, hist_range=(500, 4000),
-        check_layer=1, recompute_pct=15, seed=1001)
+        check_layer=1, recompute_pct=15, seed=1001, n_q_heads=28)
 
 
 def qwen14b() -> RoundConfig:
     return RoundConfig(
         name="qwen2.5-14b_n10_l48_h8x128_s5120", n_agents=10, n_layers=48, n_kv_heads=8,
         head_dim=128, page_size=16, block_lens=(512,) * 10, hist_range=(1000, 8000),
-        check_layer=1, recompute_pct=15, seed=1002)
+        check_layer=1, recompute_pct=15, seed=1002, n_q_heads=40)
 
 
 def scale64() -> RoundConfig:
     return RoundConfig(
         name="qwen2.5-7b_n64_l28_h4x128_s8192", n_agents=64, n_layers=28, n_kv_heads=4,
         head_dim=128, page_size=16, block_lens=(128,) * 64, hist_range=(0, 16384),
-        check_layer=1, recompute_pct=15, seed=1003)
+        check_layer=1, recompute_pct=15, seed=1003, n_q_heads=28)
 
 
 def density(pct: int, page_size: int = 16, pool_bytes: Optional[int] = 120 * 10**9) -> RoundConfig:
@@ -266,7 +267,7 @@ def density(pct: int, page_size: int = 16, pool_bytes: Optional[int] = 120 * 10*
         name=f"qwen2.5-14b_n32_l48_h8x128_s16384_p{pct}_pg{page_size}", n_agents=32,
         n_layers=48, n_kv_heads=8, head_dim=128, page_size=page_size,
         block_lens=(512,) * 32, hist_range=(1000, 8000), check_layer=1, recompute_pct=pct,
-        perturb_frac=(f, f), pool_bytes=pool_bytes, seed=1004)
+        perturb_frac=(f, f), pool_bytes=pool_bytes, seed=1004, n_q_heads=40)
 
 
 CONFIGS = {"tiny": tiny, "qwen7b": qwen7b, "qwen14b": qwen14b, "scale64": scale64}

@@ -79,3 +79,23 @@ def fresh_selected(rr, rnd: synth.Round, sel: np.ndarray, vc: torch.Tensor,
             kf[i, li] = (reused[li].float() + nk).to(torch.bfloat16)
             vf[i, li] = (vc[l - vc_layer0, tok].float() + nv).to(torch.bfloat16)
     return kf, vf
+
+
+def fill_history(rr, rnd: synth.Round, seed: Optional[int] = None):
+    """Every agent's private-history K/V (synth.history_torch) written into its pages (the
+    round must map its history pages)."""
+    cfg = rr.cfg
+    P = cfg.page_size
+    for i, h in enumerate(rnd.hist_len):
+        h = int(h)
+        if h == 0:
+            continue
+        pos = torch.arange(h, dtype=torch.int64, device=rr.device)
+        pages = rr.bt_t[i].long()[pos // P]
+        if bool((pages < 0).any()):
+            raise ValueError("history pages are not mapped")
+        for l in range(cfg.n_layers):
+            for kv, name in ((0, "K"), (1, "V")):
+                rows = synth.history_torch(cfg, i, l, name, h, rr.device, seed)
+                rr.pool_t[l, kv, pages, pos % P] = rows.view(h, cfg.n_kv_heads, cfg.head_dim)
+

@@ -97,3 +97,14 @@ def test_threaded_oracle_baseline_matches_single_threaded():
     assert np.array_equal(cache["restored"], single)
     out = bench.cpu_baseline(cfg, cfg.seed, min_seconds=0.0, max_passes=1)
     assert out["threaded"]["value"] > 0 and out["threaded"]["cores"] >= 1
+
+
+def test_attention_bytes_closed_form():
+    cfg = synth.qwen7b()
+    hist = [100, 200]
+    E, L, S = cfg.elems, cfg.n_layers, cfg.n_shared
+    rows = L * 2 * 28
+    fused = bench.attention_bytes(cfg, hist, 50, 28, from_pool=False)
+    paged = bench.attention_bytes(cfg, hist, 50, 28, from_pool=True)
+    assert fused == 300 * L * E * 4 + S * L * E * 4 + 50 * 16 * E * 4 + rows * 128 * 6 + rows * 4
+    assert paged == 300 * L * E * 4 + 2 * S * L * E * 4 + rows * 128 * 6 + rows * 4
