@@ -14,12 +14,15 @@
 //     by cp.async.bulk, 16 positions a stage, three stages in flight on an mbarrier ring.
 //     Every wait is bounded: on time-out the unit records TD_ERR_DEVICE_TIMEOUT, waits
 //     (bounded again) for the copies it issued and returns;
-//   - QK^T on the tensor cores: mma.sync m16n8k16 bf16, the head group's G <= 8 query
-//     heads as rows (rows G..15 zero). A rotated query is float32; it is split into a bf16
-//     high part and a bf16 low part, two products per k-chunk, so each score keeps 16 bits
-//     of the query (history queries are bf16 already: one product);
-//   - online softmax in base 2 per query head; PV in float32 on the CUDA cores, each lane
-//     owning D/32 dimensions of every query head's output;
+//   - both products on the tensor cores, mma.sync m16n8k16 bf16 with float32 accumulators,
+//     the head group's G <= 8 query heads as rows (rows G..15 zero). A turned query is
+//     float32: it is split into a bf16 high part and a bf16 low part, two products per
+//     k-chunk, so each score keeps 16 bits of the query (a history query is bf16 already:
+//     one product); the softmax weights are split the same way for P V;
+//   - online softmax in base 2; each lane keeps the statistics of its fragment row (query
+//     head), so rescaling needs no exchange;
+//   - the next stage's source rows are looked up before this stage's products, so the
+//     lookups' latency hides behind them;
 //   - the unit writes its partial (max, sum, unnormalised output); attn_combine_kernel
 //     merges an agent's units.
 // The same kernel with every position read from the pages (kFromPool) is plain paged
@@ -30,7 +33,7 @@ namespace td {
 
 namespace {
 
-constexpr unsigned kSpinLimit = 1u << 22;   // mbarrier polls before a unit gives up
+constexpr unsigned kSpinLimit = 1u << 20;   // mbarrier polls before a unit gives up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -80,15 +83,20 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t* r, const void* p) {
                : "r"(smem_u32(p)));
 }
 
-// D += A * B, m16n8k16, bf16 inputs, float32 accumulators. A rows g and g + 8 of the
-// thread's fragment: a0 (row g, k 0-7 pair), a2 (row g, k 8-15 pair); rows g + 8 are zero.
-__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a2, uint32_t b0,
-                                         uint32_t b1) {
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+// D += A * B, m16n8k16, bf16 inputs, float32 accumulators, all four A registers given.
+__device__ __forceinline__ void mma_bf16_full(float* d, const uint32_t* a, uint32_t b0,
+                                              uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
@@ -100,17 +108,15 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
 template <int D, bool kFromPool>
 __global__ void __launch_bounds__(32)
 attn_unit_kernel(AttnArgs A, AttnList list) {
-  constexpr int DPL = D / 32;         // output dimensions per lane
   constexpr int KCH = D / 16;         // k-chunks of one q.k product
   constexpr int RS = D * 2 + 16;      // staged row stride in bytes (conflict-free ldmatrix)
   __shared__ __align__(128) unsigned char s_k[kAttnDepth][kAttnStage * RS];
   __shared__ __align__(128) unsigned char s_v[kAttnDepth][kAttnStage * RS];
-  __shared__ __align__(16) float s_p[kAttnStage][kAttnGMax];
-  __shared__ float s_f[kAttnGMax];
   __shared__ __align__(8) uint64_t s_bar[kAttnDepth];
+  __shared__ float s_pt[kAttnStage][kAttnGMax + 1];   // softmax weights, transposed on the way
 
   const int lane = threadIdx.x;
-  const int gid = lane >> 2, tig = lane & 3;   // mma fragment row / column pair
+  const int gid = lane >> 2, tig = lane & 3;   // mma fragment group / thread in group
   const int total = list.base[list.n];
   int64_t u = blockIdx.x;
   const int c = static_cast<int>(u % total);
@@ -131,8 +137,14 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
   const int p1 = min(p0 + kAttnChunk, n_ctx);
   const int layer = A.layer_begin + li, sl = A.sl0 + li;
 
+  // rows past a partial stage are read by the products (with weight 0): keep them finite
+  for (int i = lane; i < kAttnDepth * kAttnStage * RS / 16; i += 32) {
+    reinterpret_cast<uint4*>(&s_k[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(&s_v[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   if (lane < kAttnDepth) mbar_init(&s_bar[lane], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncwarp();
 
   // the stage that starts at position p: at most 16 positions of one segment (the history,
@@ -147,64 +159,58 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
   };
   auto segment = [&](int p) { return p < hist ? -1 : __ldg(A.rd.tok_block + (p - hist)); };
 
-  // lanes 0-15 fetch the K rows, lanes 16-31 the V rows of the stage's positions
-  auto issue = [&](int k, int p) {
-    const int n = stage_end(p) - p;
+  // source row of this lane for the stage at p: lanes 0-15 the K rows, 16-31 the V rows
+  auto source = [&](int p, int n) -> const uint16_t* {
     const int tk = lane & 15, kv = lane >> 4;
-    const uint16_t* src = nullptr;
-    if (tk < n) {
-      const int pos = p + tk;
-      if (pos < hist) {
-        const int64_t row = pool_row_index(A.pool, a, layer, kv, pos, A.err);
-        if (row >= 0) src = A.pool.base + row * E + h * D;
-      } else {
-        const int t = pos - hist;
-        const int rec = __ldg(A.store.slot +
-                              (static_cast<int64_t>(a) * A.store.nl + sl) * A.rd.nb + t / A.rd.B);
-        if (rec >= A.store.capacity) {
-          atomicOr(A.err, err_bit(TD_ERR_INVALID_ARG));
-        } else if (rec >= 0) {
-          src = (kv ? A.store.val_v : A.store.val_k) +
-                (static_cast<int64_t>(rec) * A.rd.B + t % A.rd.B) * E + h * D;
-        } else {
-          src = (kv ? A.store.master_v : A.store.master_k) +
-                (static_cast<int64_t>(sl) * S + t) * E + h * D;
-        }
-      }
+    if (tk >= n) return nullptr;
+    const int pos = p + tk;
+    if (pos < hist) {
+      const int64_t row = pool_row_index(A.pool, a, layer, kv, pos, A.err);
+      return row >= 0 ? A.pool.base + row * E + h * D : nullptr;
     }
+    const int t = pos - hist;
+    const int rec = __ldg(A.store.slot +
+                          (static_cast<int64_t>(a) * A.store.nl + sl) * A.rd.nb + t / A.rd.B);
+    if (rec >= A.store.capacity) {
+      atomicOr(A.err, err_bit(TD_ERR_INVALID_ARG));
+      return nullptr;
+    }
+    if (rec >= 0)
+      return (kv ? A.store.val_v : A.store.val_k) +
+             (static_cast<int64_t>(rec) * A.rd.B + t % A.rd.B) * E + h * D;
+    return (kv ? A.store.master_v : A.store.master_k) +
+           (static_cast<int64_t>(sl) * S + t) * E + h * D;
+  };
+  auto fire = [&](int k, const uint16_t* src) {
     const unsigned ok = __ballot_sync(0xFFFFFFFFu, src != nullptr);
     uint64_t* bar = &s_bar[k % kAttnDepth];
     if (lane == 0) mbar_arrive_expect_tx(bar, __popc(ok) * (D * 2));
     __syncwarp();
     if (src)
-      bulk_g2s((kv ? s_v : s_k)[k % kAttnDepth] + tk * RS, src, D * 2, bar);
+      bulk_g2s(((lane >> 4) ? s_v : s_k)[k % kAttnDepth] + (lane & 15) * RS, src, D * 2, bar);
   };
 
-  // this lane's query values: head row gid of the group, dims kc*16 + tig*2 + {0, 1, 8, 9}
-  float qraw[KCH][4];
-  {
-    const bool live = gid < A.G;
-    const uint16_t* qrow = A.q + ((static_cast<int64_t>(li) * A.n_list + A.x0 + x) * A.nq +
-                                  h * A.G + (live ? gid : 0)) * D;
-#pragma unroll
-    for (int kc = 0; kc < KCH; ++kc) {
-      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(qrow + kc * 16 + tig * 2);
-      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(qrow + kc * 16 + tig * 2 + 8);
-      qraw[kc][0] = live ? bf_lo(w0) : 0.0f;
-      qraw[kc][1] = live ? bf_hi(w0) : 0.0f;
-      qraw[kc][2] = live ? bf_lo(w1) : 0.0f;
-      qraw[kc][3] = live ? bf_hi(w1) : 0.0f;
-    }
-  }
-  uint32_t ahi[KCH][2], alo[KCH][2];
+  // this lane's query values: head gid of the group, dims kc*16 + tig*2 + {0, 1, 8, 9}
+  // (the B operand of S^T = K Q^T: k = dims, n = query heads), read again per segment
+  const bool qlive = gid < A.G;
+  const uint16_t* qrow = A.q + ((static_cast<int64_t>(li) * A.n_list + A.x0 + x) * A.nq +
+                                h * A.G + (qlive ? gid : 0)) * D;
+  uint32_t qhi[KCH][2], qlo[KCH][2];
   bool two = false;
   // fragments of the segment's query: as given (history) or turned by R(-off_aj) (block j)
   auto build_q = [&](int seg) {
-    float v[KCH][4];
+    float qraw[KCH][4], v[KCH][4];
 #pragma unroll
-    for (int kc = 0; kc < KCH; ++kc)
+    for (int kc = 0; kc < KCH; ++kc) {
+      const uint32_t w0 = __ldg(reinterpret_cast<const unsigned int*>(qrow + kc * 16 + tig * 2));
+      const uint32_t w1 = __ldg(reinterpret_cast<const unsigned int*>(qrow + kc * 16 + tig * 2 + 8));
+      qraw[kc][0] = qlive ? bf_lo(w0) : 0.0f;
+      qraw[kc][1] = qlive ? bf_hi(w0) : 0.0f;
+      qraw[kc][2] = qlive ? bf_lo(w1) : 0.0f;
+      qraw[kc][3] = qlive ? bf_hi(w1) : 0.0f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) v[kc][i] = qraw[kc][i];
+    }
     two = seg >= 0;
     if (two) {
       const float* cs = A.rd.cos_t + static_cast<int64_t>(a * A.rd.M + seg) * (D / 2);
@@ -225,38 +231,49 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
       float hv[4], lv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint16_t hb = bf16_bits(v[kc][i]);
-        hv[i] = __uint_as_float(static_cast<uint32_t>(hb) << 16);
+        hv[i] = __uint_as_float(static_cast<uint32_t>(bf16_bits(v[kc][i])) << 16);
         lv[i] = __fsub_rn(v[kc][i], hv[i]);
       }
-      ahi[kc][0] = pack_bf2(hv[0], hv[1]);
-      ahi[kc][1] = pack_bf2(hv[2], hv[3]);
-      alo[kc][0] = pack_bf2(lv[0], lv[1]);
-      alo[kc][1] = pack_bf2(lv[2], lv[3]);
+      qhi[kc][0] = pack_bf2(hv[0], hv[1]);
+      qhi[kc][1] = pack_bf2(hv[2], hv[3]);
+      qlo[kc][0] = pack_bf2(lv[0], lv[1]);
+      qlo[kc][1] = pack_bf2(lv[2], lv[3]);
     }
   };
 
-  float o[kAttnGMax][DPL];
+  // O^T of the head group: oacc[mt] = dims mt*16 + gid (+8) x heads 2*tig, 2*tig + 1
+  float oacc[KCH][4];
 #pragma unroll
-  for (int g = 0; g < kAttnGMax; ++g)
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) o[g][d] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f;   // of query head gid (four lanes each)
+  for (int mt = 0; mt < KCH; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.0f;
+  float m_run[2] = {-INFINITY, -INFINITY};   // heads 2*tig, 2*tig + 1
+  float l_part[2] = {0.0f, 0.0f};            // this lane's share of their sums
 
   // prologue: the first stages in flight
   int ipos = p0, issued = 0;
   for (int k = 0; k < kAttnDepth && ipos < p1; ++k) {
-    issue(k, ipos);
-    ipos = stage_end(ipos);
+    const int e = stage_end(ipos);
+    fire(k, source(ipos, e - ipos));
+    ipos = e;
     ++issued;
   }
   int cseg = -2;
   int cpos = p0;
   bool failed = false;
+  // ldmatrix row addresses: K as the A operand (rows = positions), V transposed (rows = dims)
+  const int koff = (((lane >> 3) & 1) * 8 + (lane & 7)) * RS + (lane >> 4) * 16;
+  const int voff = ((lane >> 4) * 8 + (lane & 7)) * RS + ((lane >> 3) & 1) * 16;
   for (int k = 0; cpos < p1; ++k) {
     const int cend = stage_end(cpos);
     const int n = cend - cpos;
     const int buf = k % kAttnDepth;
+    // the next stage's rows are looked up now, their copies fired after this stage
+    const bool more = ipos < p1;
+    int iend = ipos;
+    const uint16_t* nsrc = nullptr;
+    if (more) {
+      iend = stage_end(ipos);
+      nsrc = source(ipos, iend - ipos);
+    }
     if (!mbar_wait_bounded(&s_bar[buf], (k / kAttnDepth) & 1)) {
       failed = true;
       if (lane == 0) atomicOr(A.err, err_bit(TD_ERR_DEVICE_TIMEOUT));
@@ -269,98 +286,96 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
       build_q(seg);
       cseg = seg;
     }
-    // scores of head gid for positions nt*8 + tig*2 + {0, 1}
-    float s2[2][2];
+    // S^T = K Q^T: positions gid, gid + 8 x heads 2*tig, 2*tig + 1; two chains (high, low)
+    float sh[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sl2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const unsigned char* kb = s_k[buf] + koff;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      const unsigned char* kb = s_k[buf] + (nt * 8 + (lane & 7)) * RS + (lane >> 4) * 32 +
-                                ((lane >> 3) & 1) * 16;
-#pragma unroll
-      for (int cp = 0; cp < KCH / 2; ++cp) {
-        uint32_t b[4];
-        ldmatrix_x4(b, kb + cp * 64);
-        mma_bf16(acc, ahi[2 * cp][0], ahi[2 * cp][1], b[0], b[1]);
-        mma_bf16(acc, ahi[2 * cp + 1][0], ahi[2 * cp + 1][1], b[2], b[3]);
-        if (two) {
-          mma_bf16(acc, alo[2 * cp][0], alo[2 * cp][1], b[0], b[1]);
-          mma_bf16(acc, alo[2 * cp + 1][0], alo[2 * cp + 1][1], b[2], b[3]);
-        }
-      }
-#pragma unroll
-      for (int col = 0; col < 2; ++col) {
-        const bool valid = gid < A.G && nt * 8 + tig * 2 + col < n;
-        s2[nt][col] = valid ? acc[col] * A.scale_log2 : -INFINITY;
-      }
+    for (int kc = 0; kc < KCH; ++kc) {
+      uint32_t af[4];
+      ldmatrix_x4(af, kb + kc * 32);
+      mma_bf16_full(sh, af, qhi[kc][0], qhi[kc][1]);
+      if (two) mma_bf16_full(sl2, af, qlo[kc][0], qlo[kc][1]);
     }
-    float smax = fmaxf(fmaxf(s2[0][0], s2[0][1]), fmaxf(s2[1][0], s2[1][1]));
-    smax = fmaxf(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, 1));
-    smax = fmaxf(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, 2));
-    const float m_new = fmaxf(m_run, smax);
-    const float fac = m_run == -INFINITY ? 0.0f : exp2f(m_run - m_new);
-    float psum = 0.0f;
+    // scores (base 2) of (position r, head c): r = gid + 8 * (i >> 1), c = 2 * tig + (i & 1)
+    float s2[4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int i = 0; i < 4; ++i) {
+      const bool valid = 2 * tig + (i & 1) < A.G && gid + 8 * (i >> 1) < n;
+      s2[i] = valid ? __fadd_rn(sh[i], sl2[i]) * A.scale_log2 : -INFINITY;
+    }
+    float fac[2], p[4];
 #pragma unroll
-      for (int col = 0; col < 2; ++col) {
-        const float p = s2[nt][col] == -INFINITY ? 0.0f : exp2f(s2[nt][col] - m_new);
-        psum += p;
-        s_p[nt * 8 + tig * 2 + col][gid] = p;
-      }
-    psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 1);
-    psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 2);
-    l_run = __fmaf_rn(l_run, fac, psum);
-    m_run = m_new;
-    if (tig == 0) s_f[gid] = fac;
+    for (int c2 = 0; c2 < 2; ++c2) {
+      float mx = fmaxf(s2[c2], s2[c2 + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+      const float m_new = fmaxf(m_run[c2], mx);
+      fac[c2] = m_run[c2] == -INFINITY ? 0.0f : exp2f(m_run[c2] - m_new);
+      p[c2] = s2[c2] == -INFINITY ? 0.0f : exp2f(s2[c2] - m_new);
+      p[c2 + 2] = s2[c2 + 2] == -INFINITY ? 0.0f : exp2f(s2[c2 + 2] - m_new);
+      l_part[c2] = __fmaf_rn(l_part[c2], fac[c2], p[c2] + p[c2 + 2]);
+      m_run[c2] = m_new;
+    }
+    // P^T as the B operand of O^T += V^T P^T (k = positions, n = heads): transposed
+    // through shared memory, then split into two bf16 parts like the query
+    s_pt[gid][2 * tig] = p[0];
+    s_pt[gid][2 * tig + 1] = p[1];
+    s_pt[gid + 8][2 * tig] = p[2];
+    s_pt[gid + 8][2 * tig + 1] = p[3];
     __syncwarp();
-    // PV: every query head's output over this lane's dimensions
+    const float pt[4] = {s_pt[2 * tig][gid], s_pt[2 * tig + 1][gid], s_pt[2 * tig + 8][gid],
+                         s_pt[2 * tig + 9][gid]};
+    float ph[4];
 #pragma unroll
-    for (int g = 0; g < kAttnGMax; ++g) {
-      const float f = s_f[g];
+    for (int i = 0; i < 4; ++i)
+      ph[i] = __uint_as_float(static_cast<uint32_t>(bf16_bits(pt[i])) << 16);
+    const uint32_t bh0 = pack_bf2(ph[0], ph[1]), bh1 = pack_bf2(ph[2], ph[3]);
+    const uint32_t bl0 = pack_bf2(__fsub_rn(pt[0], ph[0]), __fsub_rn(pt[1], ph[1]));
+    const uint32_t bl1 = pack_bf2(__fsub_rn(pt[2], ph[2]), __fsub_rn(pt[3], ph[3]));
+    const unsigned char* vb = s_v[buf] + voff;
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) o[g][d] *= f;
+    for (int mt = 0; mt < KCH; ++mt) {
+      uint32_t af[4];
+      ldmatrix_x4_trans(af, vb + mt * 32);
+      oacc[mt][0] *= fac[0];
+      oacc[mt][1] *= fac[1];
+      oacc[mt][2] *= fac[0];
+      oacc[mt][3] *= fac[1];
+      mma_bf16_full(oacc[mt], af, bh0, bh1);
+      mma_bf16_full(oacc[mt], af, bl0, bl1);
     }
-    const unsigned char* vb = s_v[buf] + lane * DPL * 2;
-    for (int t = 0; t < n; ++t) {
-      const float4 pa = *reinterpret_cast<const float4*>(&s_p[t][0]);
-      const float4 pb = *reinterpret_cast<const float4*>(&s_p[t][4]);
-      const float pg[kAttnGMax] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-      float vv[DPL];
-      if constexpr (DPL == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(vb + t * RS);
-        vv[0] = bf_lo(w.x);
-        vv[1] = bf_hi(w.x);
-        vv[2] = bf_lo(w.y);
-        vv[3] = bf_hi(w.y);
-      } else {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(vb + t * RS);
-        vv[0] = bf_lo(w);
-        vv[1] = bf_hi(w);
-      }
-#pragma unroll
-      for (int g = 0; g < kAttnGMax; ++g)
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) o[g][d] = __fmaf_rn(pg[g], vv[d], o[g][d]);
-    }
-    __syncwarp();   // this stage's buffers and s_p, s_f are no longer read
+    __syncwarp();   // this stage's buffers and s_pt are no longer read
     cpos = cend;
-    if (ipos < p1) {
+    if (more) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(issued, ipos);
-      ipos = stage_end(ipos);
+      fire(issued, nsrc);
+      ipos = iend;
       ++issued;
     }
   }
   if (failed) return;
+#pragma unroll
+  for (int c2 = 0; c2 < 2; ++c2) {
+    l_part[c2] += __shfl_xor_sync(0xFFFFFFFFu, l_part[c2], 4);
+    l_part[c2] += __shfl_xor_sync(0xFFFFFFFFu, l_part[c2], 8);
+    l_part[c2] += __shfl_xor_sync(0xFFFFFFFFu, l_part[c2], 16);
+  }
   const int64_t unit = blockIdx.x;
-  float* po = A.part_o + unit * kAttnGMax * D + lane * DPL;
+  float* po = A.part_o + unit * kAttnGMax * D;
 #pragma unroll
-  for (int g = 0; g < kAttnGMax; ++g)
+  for (int mt = 0; mt < KCH; ++mt) {
+    po[(2 * tig) * D + mt * 16 + gid] = oacc[mt][0];
+    po[(2 * tig + 1) * D + mt * 16 + gid] = oacc[mt][1];
+    po[(2 * tig) * D + mt * 16 + gid + 8] = oacc[mt][2];
+    po[(2 * tig + 1) * D + mt * 16 + gid + 8] = oacc[mt][3];
+  }
+  if (gid == 0) {
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) po[g * D + d] = o[g][d];
-  if (tig == 0) {
-    A.part_ml[(unit * kAttnGMax + gid) * 2] = m_run;
-    A.part_ml[(unit * kAttnGMax + gid) * 2 + 1] = l_run;
+    for (int c2 = 0; c2 < 2; ++c2) {
+      A.part_ml[(unit * kAttnGMax + 2 * tig + c2) * 2] = m_run[c2];
+      A.part_ml[(unit * kAttnGMax + 2 * tig + c2) * 2 + 1] = l_part[c2];
+    }
   }
 }
 
