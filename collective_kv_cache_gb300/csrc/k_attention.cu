@@ -11,7 +11,8 @@
 //
 // Work unit = (layer, kv head, agent, 512 positions of the agent's context), one warp:
 //   - each position's K and V rows of the head (D bf16 each) are staged in shared memory
-//     by cp.async.bulk, 16 positions a stage, three stages in flight on an mbarrier ring.
+//     by cp.async.bulk, 16 positions a stage, on a ring of two stages with mbarriers (two
+//     stages keep the shared memory at 17 KB a warp, so twelve warps fit on an SM).
 //     Every wait is bounded: on time-out the unit records TD_ERR_DEVICE_TIMEOUT, waits
 //     (bounded again) for the copies it issued and returns;
 //   - both products on the tensor cores, mma.sync m16n8k16 bf16 with float32 accumulators,
@@ -106,7 +107,7 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
 }  // namespace
 
 template <int D, bool kFromPool>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(32, 12)
 attn_unit_kernel(AttnArgs A, AttnList list) {
   constexpr int KCH = D / 16;         // k-chunks of one q.k product
   constexpr int RS = D * 2 + 16;      // staged row stride in bytes (conflict-free ldmatrix)
@@ -286,22 +287,27 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
       build_q(seg);
       cseg = seg;
     }
-    // S^T = K Q^T: positions gid, gid + 8 x heads 2*tig, 2*tig + 1; two chains (high, low)
-    float sh[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sl2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // S^T = K Q^T: positions gid, gid + 8 x heads 2*tig, 2*tig + 1; four independent
+    // chains (high / low part of the query x even / odd k-chunks)
+    float sacc[4][4];
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) sacc[ch][0] = sacc[ch][1] = sacc[ch][2] = sacc[ch][3] = 0.0f;
     const unsigned char* kb = s_k[buf] + koff;
 #pragma unroll
     for (int kc = 0; kc < KCH; ++kc) {
       uint32_t af[4];
       ldmatrix_x4(af, kb + kc * 32);
-      mma_bf16_full(sh, af, qhi[kc][0], qhi[kc][1]);
-      if (two) mma_bf16_full(sl2, af, qlo[kc][0], qlo[kc][1]);
+      mma_bf16_full(sacc[kc & 1], af, qhi[kc][0], qhi[kc][1]);
+      if (two) mma_bf16_full(sacc[2 + (kc & 1)], af, qlo[kc][0], qlo[kc][1]);
     }
     // scores (base 2) of (position r, head c): r = gid + 8 * (i >> 1), c = 2 * tig + (i & 1)
     float s2[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const bool valid = 2 * tig + (i & 1) < A.G && gid + 8 * (i >> 1) < n;
-      s2[i] = valid ? __fadd_rn(sh[i], sl2[i]) * A.scale_log2 : -INFINITY;
+      const float sc = __fadd_rn(__fadd_rn(sacc[0][i], sacc[1][i]),
+                                 __fadd_rn(sacc[2][i], sacc[3][i]));
+      s2[i] = valid ? sc * A.scale_log2 : -INFINITY;
     }
     float fac[2], p[4];
 #pragma unroll

@@ -131,7 +131,7 @@ cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& poo
 // Decode attention from the Master and the diffs (k_attention.cu).
 constexpr int kAttnChunk = 512;    // context positions per work unit (one warp)
 constexpr int kAttnStage = 16;     // positions per pipeline stage
-constexpr int kAttnDepth = 3;      // stages in flight per unit
+constexpr int kAttnDepth = 2;      // stages in flight per unit
 constexpr int kAttnGMax = 8;       // query heads per kv head
 
 struct AttnList {
