@@ -17,8 +17,10 @@
 //           diff blocks (a 32-token block is two tiles): reads its canonical data
 //           once, builds the Master's (recomputed K turned back by R(-off)) and writes it,
 //           then for each candidate Mirror builds its data, writes it at its candidate
-//           place and ORs "differs" into the block's flag, one atomic per warp; the warp
-//           that sets a flag first counts the record in its row. One CTA per block writes
+//           place and notes in shared memory whether it differs (one warp vote); after
+//           the candidates, one thread per differing candidate ORs the block's flag and,
+//           if it set the flag first, counts the record in its row (the atomics' round
+//           trips overlap instead of following each candidate). One CTA per block writes
 //           the slot map and block indices of the common case (every candidate kept);
 //           the CTA that finishes last turns the record counts into rowptr.
 //   fixup   only when some candidate equalled the Master's block: compacts the slot map
@@ -337,6 +339,7 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
   __shared__ unsigned s_bits[kAgentChunk];
   __shared__ int s_first[kAgentChunk];
   __shared__ int s_list[kAgentChunk];        // the chunk's candidates, in agent order
+  __shared__ unsigned s_diff[kAgentChunk];   // candidate j of the list differs somewhere
   __shared__ int s_nc;
   extern __shared__ uint4 s_stage[];         // [kStageDepth][2][kItems][blockDim]
   const int slot_cells = 2 * kItems * blockDim.x;
@@ -378,6 +381,7 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
       }
       if (threadIdx.x == 0) s_nc = nc;
     }
+    for (int j = threadIdx.x; j < kAgentChunk; j += blockDim.x) s_diff[j] = 0u;
     __syncthreads();
     const int nc = s_nc;
     // pipeline: candidates j+1 .. j+depth-1 are being staged while j is built and stored
@@ -418,13 +422,19 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
           store_item<kItems>(a, kv, rec, h, r, z, z);
         }
       }
-      if (__any_sync(0xFFFFFFFFu, d) && lane == 0) {
-        const int64_t f = (static_cast<int64_t>(i) * a.nl + li) * nb + b;
-        if (atomicOr(a.sc.flag + f, 1u) == 0u)
-          atomicAdd(a.sc.row_count + static_cast<int64_t>(i) * a.nl + li, 1);
-      }
+      if (__any_sync(0xFFFFFFFFu, d) && lane == 0) s_diff[j] = 1u;   // same value from all
     }
     cp_async_wait<0>();
+    // the chunk's verdicts: one global flag per candidate that differs, set in parallel;
+    // whoever sets a flag first (this CTA or the other half's) counts the record
+    __syncthreads();
+    for (int j = threadIdx.x; j < nc; j += blockDim.x) {
+      if (!s_diff[j]) continue;
+      const int i = c0 + s_list[j];
+      const int64_t f = (static_cast<int64_t>(i) * a.nl + li) * nb + b;
+      if (atomicOr(a.sc.flag + f, 1u) == 0u)
+        atomicAdd(a.sc.row_count + static_cast<int64_t>(i) * a.nl + li, 1);
+    }
   }
   // the CTA that finishes last turns the record counts into rowptr
   __shared__ int s_last;
