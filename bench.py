@@ -33,7 +33,7 @@ if ROOT not in sys.path:
 
 METRIC = "restore+reuse KV GB/s (% of GB300 HBM peak); agent-rounds/sec, 7B shape"
 UNIT = "GB/s"
-LAUNCHES_PER_STEP = 8    # rerotate 1, deviation + top-k 2, master 1, encode 3, restore 1
+LAUNCHES_PER_STEP = 9    # rerotate 1, deviation + top-k 2, master 1, encode 4, restore 1
 # DRAM bytes (read + write) per launch of the roofline kernels at the benchmarked size, from
 # one ncu capture of these kernels as they are now (dram__bytes_read.sum +
 # dram__bytes_write.sum); set an entry to None when its kernel changes.

@@ -6,7 +6,7 @@
 // Only blocks that hold a selected token of the Mirror or of the Master can differ (every
 // other token of both is the canonical K/V itself), so the candidate blocks of Mirror i
 // are mask_i | mask_master. Their number per layer is known before any K/V is read, which
-// gives every candidate block a fixed place in the store. Three launches:
+// gives every candidate block a fixed place in the store. Four launches:
 //   prep    one CTA per agent: zeroes the agent's flags and record counts, builds a
 //           mask of its selected tokens in each diff block (16 or 32 bits), the rank of the
 //           block's first selected token and its block bitmask; the CTA that finishes
@@ -18,11 +18,11 @@
 //           once, builds the Master's (recomputed K turned back by R(-off)) and writes it,
 //           then for each candidate Mirror builds its data, writes it at its candidate
 //           place and notes in shared memory whether it differs (one warp vote); after
-//           the candidates, one thread per differing candidate ORs the block's flag and,
-//           if it set the flag first, counts the record in its row (the atomics' round
-//           trips overlap instead of following each candidate). One CTA per block writes
-//           the slot map and block indices of the common case (every candidate kept);
-//           the CTA that finishes last turns the record counts into rowptr.
+//           the candidates, one thread per differing candidate ORs the block's flag,
+//           without waiting for the result. One CTA per block writes the slot map and
+//           block indices of the common case (every candidate kept);
+//   rows    one CTA: each (agent, layer) row's record count from its flags, one warp a
+//           row, then their prefix sum -> rowptr, and whether the fix-up must run;
 //   fixup   only when some candidate equalled the Master's block: compacts the slot map
 //           and indices and rewrites the kept blocks whose record moved (recomputed from
 //           the inputs, never copied); otherwise it returns at once.
@@ -108,7 +108,6 @@ __global__ void __launch_bounds__(1024) enc_prep_kernel(EncArgs a, const int32_t
   const int32_t* sel = a.sel + static_cast<int64_t>(i) * k;
   uint32_t* flags = a.sc.flag + static_cast<int64_t>(i) * a.nl * nb;
   for (int x = threadIdx.x; x < a.nl * nb; x += blockDim.x) flags[x] = 0u;
-  for (int x = threadIdx.x; x < a.nl; x += blockDim.x) a.sc.row_count[i * a.nl + x] = 0;
   for (int b = threadIdx.x; b < nb; b += blockDim.x) bits[b] = 0u;
   for (int w = threadIdx.x; w < nbw; w += blockDim.x) smask[w] = 0u;
   __syncthreads();
@@ -425,28 +424,32 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
       if (__any_sync(0xFFFFFFFFu, d) && lane == 0) s_diff[j] = 1u;   // same value from all
     }
     cp_async_wait<0>();
-    // the chunk's verdicts: one global flag per candidate that differs, set in parallel;
-    // whoever sets a flag first (this CTA or the other half's) counts the record
+    // the chunk's verdicts: one global flag per candidate that differs, set in parallel
+    // and without waiting for the result (the other half-tile may set it too)
     __syncthreads();
     for (int j = threadIdx.x; j < nc; j += blockDim.x) {
       if (!s_diff[j]) continue;
       const int i = c0 + s_list[j];
-      const int64_t f = (static_cast<int64_t>(i) * a.nl + li) * nb + b;
-      if (atomicOr(a.sc.flag + f, 1u) == 0u)
-        atomicAdd(a.sc.row_count + static_cast<int64_t>(i) * a.nl + li, 1);
+      atomicOr(a.sc.flag + (static_cast<int64_t>(i) * a.nl + li) * nb + b, 1u);
     }
   }
-  // the CTA that finishes last turns the record counts into rowptr
-  __shared__ int s_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(a.main_done, 1) == static_cast<int>(gridDim.x) - 1;
+}
+
+// One CTA after the main kernel: every (agent, layer) row's record count from the flags
+// (one warp per row), then their exclusive prefix sum -> rowptr and the fix-up decision.
+__global__ void __launch_bounds__(1024) enc_rows_kernel(EncArgs a) {
+  if (*a.m_ok < 0) return;
+  const int R = a.rd.N * a.nl, nb = a.rd.nb;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int r = wid; r < R; r += nw) {
+    const uint32_t* f = a.sc.flag + static_cast<int64_t>(r) * nb;
+    int cnt = 0;
+    for (int b = lane; b < nb; b += 32) cnt += __ldcg(f + b) != 0u;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+    if (lane == 0) a.sc.row_count[r] = cnt;
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (threadIdx.x == 0) *a.main_done = 0;     // ready for the next call
   rows_prefix(a);
 }
 
@@ -532,6 +535,8 @@ static cudaError_t run_tiles(const EncArgs& a, int threads, cudaStream_t st) {
   enc_main_kernel<kItems><<<static_cast<unsigned>(units), threads, stage, st>>>(a, tpl);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  enc_rows_kernel<<<1, 1024, 0, st>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   enc_fixup_kernel<kItems><<<152, 256, 0, st>>>(a, tpl);
   return cudaGetLastError();
 }
