@@ -88,6 +88,20 @@ def stage_bytes(cfg, n_agents: int, nl: int, k: int, nnz: int, n_restored: int) 
     }
 
 
+def storage_ratios(cfg, nnz: int, nl: int) -> dict:
+    """Compression of the round's Master-Mirror store in closed form ([R] §7a: dense KV over
+    Master + diffs). One dense agent is nl*S*E bf16 for K and again for V; a diff record
+    costs its K and V values plus a 4-byte index; the row pointers 8 bytes each."""
+    N, S, E, B = cfg.n_agents, cfg.n_shared, cfg.elems, cfg.diff_block
+    dense = nl * S * E * 2 * 2
+    rec = B * E * 4 + 4
+    store = dense + nnz * rec + 8 * (N * nl + 1)
+    per_mirror = dense * (N - 1) / (nnz * rec) if nnz and N > 1 else None
+    return {"records": int(nnz), "round_ratio": round(N * dense / store, 3),
+            "caches_for_all_agents": round(store / dense, 3),
+            "per_mirror_ratio": None if per_mirror is None else round(per_mirror, 3)}
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -446,6 +460,8 @@ def bench_ours(args, rank, world, local_rank):
             "stages": {n: {"ms": round(stage_ms[n], 5), "bytes": by[n],
                            "gbs": round(by[n] / (stage_ms[n] * 1e-3) / 1e9, 1)} for n in STAGES},
             "diff_blocks": st["nnz"], "selected_per_agent": st["k"], "master": st["master"],
+            "storage": storage_ratios(cfg, st["nnz"], L),
+            "restore_us_per_agent_layer": round(stage_ms["restore"] * 1e3 / (N * L), 4),
             "host_link": None if not args.store_on_host else {
                 "restore_reads_gbs": round((2 * L * cfg.n_shared * cfg.elems * 2 + st["nnz"] *
                                             (cfg.diff_block * cfg.elems * 4 + 4)) / (stage_ms["restore"] * 1e-3) / 1e9, 1),

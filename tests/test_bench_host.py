@@ -108,3 +108,15 @@ def test_attention_bytes_closed_form():
     paged = bench.attention_bytes(cfg, hist, 50, 28, from_pool=True)
     assert fused == 300 * L * E * 4 + S * L * E * 4 + 50 * 16 * E * 4 + rows * 128 * 6 + rows * 4
     assert paged == 300 * L * E * 4 + 2 * S * L * E * 4 + rows * 128 * 6 + rows * 4
+
+
+def test_storage_ratios_match_the_oracle_closed_form():
+    """The bench's ratios against the oracle's own closed forms (pinned to the pages'
+    storage table by the oracle pins)."""
+    import oracle
+    cfg = synth.qwen7b()
+    orc = oracle.get()
+    nnz = 22456
+    r = bench.storage_ratios(cfg, nnz, cfg.n_layers)
+    assert abs(r["round_ratio"] - orc.round_ratio(cfg, nnz)) < 1e-3
+    assert abs(r["per_mirror_ratio"] - orc.mirror_ratio(cfg, nnz // (cfg.n_agents - 1))) < 0.05
