@@ -660,8 +660,11 @@ def report_chunked(args, cfg, seed, device, rank, world):
 
 
 def bench_e2e(st, agents, cfg, K, device, args):
-    """Same step through the public calls with HOST inputs: pinned host -> device copies of
-    the round's inputs and a device -> host read of its result inside the timed region."""
+    """Same step through the public calls with HOST inputs: every step's inputs are copied
+    from pinned host memory to the device and its result (row pointers, selection, master)
+    read back to the host, inside the timed region. The copies run on their own stream into
+    two alternating sets of device inputs, so step i + 1's inputs travel while step i
+    computes; each copy still waits until the step that last used its set has finished."""
     import torch
 
     rr = st["rr"]
@@ -669,30 +672,49 @@ def bench_e2e(st, agents, cfg, K, device, args):
     host = {n: torch.empty(st[n].shape, dtype=st[n].dtype, pin_memory=True) for n in names}
     for n in names:
         host[n].copy_(st[n])
+    sets = [{n: st[n] for n in names}, {n: torch.empty_like(st[n]) for n in names}]
     res = {"rowptr": rr.store_t["rowptr"], "sel": rr.sel_t, "master": rr.master_t}
     res_h = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in res.items()}
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = sum(t.numel() * t.element_size() for t in res.values())
     s = rr.stream
+    cs = torch.cuda.Stream(device)
     side = torch.cuda.Stream(device, priority=-1)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    used = [torch.cuda.Event(), torch.cuda.Event()]
 
-    def one():
-        with torch.cuda.stream(s):
+    def copy_in(i):
+        k = i % 2
+        cs.wait_event(used[k])
+        with torch.cuda.stream(cs):
             for n in names:
-                st[n].copy_(host[n], non_blocking=True)
-        run_overlapped(st, agents, side, torch.cuda.Event(), torch.cuda.Event(), args)
+                sets[k][n].copy_(host[n], non_blocking=True)
+        copied[k].record(cs)
+
+    def compute(i):
+        k = i % 2
+        s.wait_event(copied[k])
+        run_overlapped(dict(st, **sets[k]), agents, side, torch.cuda.Event(), torch.cuda.Event(),
+                       args)
+        used[k].record(s)
         with torch.cuda.stream(s):
             for n, t in res.items():
                 res_h[n].copy_(t, non_blocking=True)
+
+    def steps(n):
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            compute(i)
         s.synchronize()
 
-    for _ in range(2):
-        one()
+    steps(3)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(s)
-    for _ in range(K):
-        one()
+    cs.wait_event(a)
+    steps(K)
     b.record(s)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
@@ -700,7 +722,9 @@ def bench_e2e(st, agents, cfg, K, device, args):
                          cfg.n_agents).values())
     return {"value": round(by * K / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "ms_per_step": round(ms / K, 4), "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h)}
+            "d2h_bytes_per_step": int(d2h),
+            "copies": "a copy stream, two alternating input sets: step i+1's inputs travel "
+                      "while step i computes"}
 
 
 # ------------------------------------------------------------------ the oracle on host cores
