@@ -441,13 +441,21 @@ __global__ void __launch_bounds__(1024) enc_rows_kernel(EncArgs a) {
   if (*a.m_ok < 0) return;
   const int R = a.rd.N * a.nl, nb = a.rd.nb;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int r = wid; r < R; r += nw) {
-    const uint32_t* f = a.sc.flag + static_cast<int64_t>(r) * nb;
-    int cnt = 0;
-    for (int b = lane; b < nb; b += 32) cnt += __ldcg(f + b) != 0u;
+  constexpr int kRows = 4;   // rows a warp counts at once: their loads are all in flight
+  for (int r0 = wid * kRows; r0 < R; r0 += nw * kRows) {
+    int cnt[kRows];
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
-    if (lane == 0) a.sc.row_count[r] = cnt;
+    for (int q = 0; q < kRows; ++q) cnt[q] = 0;
+    for (int b = lane; b < nb; b += 32)
+#pragma unroll
+      for (int q = 0; q < kRows; ++q)
+        if (r0 + q < R) cnt[q] += __ldcg(a.sc.flag + static_cast<int64_t>(r0 + q) * nb + b) != 0u;
+#pragma unroll
+    for (int q = 0; q < kRows; ++q) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) cnt[q] += __shfl_xor_sync(0xFFFFFFFFu, cnt[q], o);
+      if (lane == 0 && r0 + q < R) a.sc.row_count[r0 + q] = cnt[q];
+    }
   }
   __syncthreads();
   rows_prefix(a);
