@@ -394,15 +394,37 @@ def bench_ours(args, rank, world, local_rank):
     ev_m = [torch.cuda.Event() for _ in range(K)]
     for _ in range(2):                      # the overlapped schedule, warmed too
         run_overlapped(st, agents, side, torch.cuda.Event(), torch.cuda.Event(), args)
+    graph = None
+    if not args.no_graph:
+        # one step's launches (both streams) captured once and replayed per step; the
+        # round's tables are already on the device, so the calls make no host round trips
+        torch.cuda.synchronize()
+        main_stream = rr.stream
+        rr.stream = torch.cuda.Stream(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=rr.stream):
+            run_overlapped(st, agents, side, torch.cuda.Event(), torch.cuda.Event(), args)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(rr.stream):
+            for _ in range(2):
+                graph.replay()
+        torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     start.record(rr.stream)
-    for i in range(K):
-        run_overlapped(st, agents, side, ev_c[i], ev_m[i], args)
+    if graph is not None:
+        with torch.cuda.stream(rr.stream):
+            for i in range(K):
+                graph.replay()
+    else:
+        for i in range(K):
+            run_overlapped(st, agents, side, ev_c[i], ev_m[i], args)
     end.record(rr.stream)
     torch.cuda.synchronize()
+    if graph is not None:
+        rr.stream = main_stream
     clk.mark("load_end")
     clk.__exit__(None, None, None)
     if world > 1:
@@ -473,9 +495,11 @@ def bench_ours(args, rank, world, local_rank):
             "e2e": e2e,
             "gpu_launches": (LAUNCHES_PER_STEP + (0 if args.sequential else
                              (cfg.check_layer > 0) + (cfg.check_layer + 1 < L))) * K,
-            "schedule": "sequential" if args.sequential else
-                        "check layer first; selection and master on a second stream "
-                        "overlapped with the other layers' re-rotation",
+            "schedule": ("sequential" if args.sequential else
+                         "check layer first; selection and master on a second stream "
+                         "overlapped with the other layers' re-rotation") +
+                        ("" if args.no_graph else "; one step captured in a CUDA graph, "
+                         "replayed per step"),
             "stages_sequential_ms": round(seq_ms, 5),
             "clocks": clk.summary(),
             "comparisons": comparisons,
@@ -906,6 +930,9 @@ def main(argv=None):
                     help="skip the serial-PIC and dense-restore comparison baselines")
     ap.add_argument("--no-attention", action="store_true",
                     help="skip the fused-attention measurement")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every step's kernels from the host instead of replaying a "
+                         "captured CUDA graph")
     ap.add_argument("--cpu-layers", type=int, default=None)
     ap.add_argument("--ref-layers", type=int, default=4)
     args = ap.parse_args(argv)
