@@ -346,30 +346,33 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
   for (int c0 = 0; c0 < N; c0 += kAgentChunk) {
     const int n = min(kAgentChunk, N - c0);
     if (c0 > 0) __syncthreads();
-    for (int x = threadIdx.x; x < n; x += blockDim.x) {
-      const int i = c0 + x;
-      // all facts loaded at once (one round trip); unused ones are simply ignored
-      const unsigned word = a.sc.cand[i * nbw + (b >> 5)];
-      const unsigned sb = a.sc.selbits[static_cast<int64_t>(i) * nb + b];
-      const int fr = a.sc.firstrank[static_cast<int64_t>(i) * nb + b];
-      const int64_t ap0 = a.sc.agent_prefix[i], ap1 = a.sc.agent_prefix[i + 1];
-      const int wp = a.sc.word_prefix[i * nbw + (b >> 5)];
-      const bool is_cand = (word >> (b & 31)) & 1u;
-      const unsigned below = (b & 31) ? (word & ((1u << (b & 31)) - 1u)) : 0u;
-      const int64_t place = is_cand ? ap0 * a.nl + static_cast<int64_t>(li) * (ap1 - ap0) + wp +
-                                          __popc(below)
-                                    : -1;
-      const unsigned ibits = is_cand ? sb : 0u;
-      s_place[x] = place;
-      s_bits[x] = ibits;
-      s_first[x] = ibits ? fr : 0;
-      if (designated && !over) {   // slot map and index of the common case
-        a.store.slot[(static_cast<int64_t>(i) * a.nl + li) * nb + b] = static_cast<int32_t>(place);
-        if (place >= 0) a.store.block_idx[place] = b;
+    if (threadIdx.x < 32) {
+      // the first warp alone: the chunk's per-agent facts (all loaded in one round trip;
+      // unused ones are ignored), then the candidates compacted in agent order
+      for (int x = threadIdx.x; x < n; x += 32) {
+        const int i = c0 + x;
+        const unsigned word = a.sc.cand[i * nbw + (b >> 5)];
+        const unsigned sb = a.sc.selbits[static_cast<int64_t>(i) * nb + b];
+        const int fr = a.sc.firstrank[static_cast<int64_t>(i) * nb + b];
+        const int64_t ap0 = a.sc.agent_prefix[i], ap1 = a.sc.agent_prefix[i + 1];
+        const int wp = a.sc.word_prefix[i * nbw + (b >> 5)];
+        const bool is_cand = (word >> (b & 31)) & 1u;
+        const unsigned below = (b & 31) ? (word & ((1u << (b & 31)) - 1u)) : 0u;
+        const int64_t place = is_cand ? ap0 * a.nl + static_cast<int64_t>(li) * (ap1 - ap0) +
+                                            wp + __popc(below)
+                                      : -1;
+        const unsigned ibits = is_cand ? sb : 0u;
+        s_place[x] = place;
+        s_bits[x] = ibits;
+        s_first[x] = ibits ? fr : 0;
+        s_diff[x] = 0u;
+        if (designated && !over) {   // slot map and index of the common case
+          a.store.slot[(static_cast<int64_t>(i) * a.nl + li) * nb + b] =
+              static_cast<int32_t>(place);
+          if (place >= 0) a.store.block_idx[place] = b;
+        }
       }
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {                    // compact the candidates, in agent order
+      __syncwarp();
       int nc = 0;
       for (int x0 = 0; x0 < n; x0 += 32) {
         const int x = x0 + threadIdx.x;
@@ -380,7 +383,6 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
       }
       if (threadIdx.x == 0) s_nc = nc;
     }
-    for (int j = threadIdx.x; j < kAgentChunk; j += blockDim.x) s_diff[j] = 0u;
     __syncthreads();
     const int nc = s_nc;
     // pipeline: candidates j+1 .. j+depth-1 are being staged while j is built and stored
