@@ -102,6 +102,22 @@ def storage_ratios(cfg, nnz: int, nl: int) -> dict:
             "per_mirror_ratio": None if per_mirror is None else round(per_mirror, 3)}
 
 
+def diff_density(cfg, rowptr, master: int, nl: int) -> dict:
+    """Records per (Mirror, layer), from the store's row pointers: how many of a layer's
+    diff blocks each Mirror had to keep (the pages' "changed blocks per Mirror")."""
+    N = cfg.n_agents
+    nb = (cfg.n_shared + cfg.diff_block - 1) // cfg.diff_block
+    rp = np.asarray(rowptr, dtype=np.int64)
+    per = np.diff(rp).reshape(N, nl)
+    mir = np.delete(per, master, axis=0).reshape(-1) if N > 1 else per.reshape(-1)
+    if mir.size == 0:
+        return None
+    q = np.percentile(mir, [10, 50, 90])
+    return {"blocks_per_layer": nb, "mean": round(float(mir.mean()), 2),
+            "p10": float(q[0]), "p50": float(q[1]), "p90": float(q[2]),
+            "max": int(mir.max()), "changed_fraction": round(float(mir.mean()) / nb, 4)}
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -483,6 +499,7 @@ def bench_ours(args, rank, world, local_rank):
                            "gbs": round(by[n] / (stage_ms[n] * 1e-3) / 1e9, 1)} for n in STAGES},
             "diff_blocks": st["nnz"], "selected_per_agent": st["k"], "master": st["master"],
             "storage": storage_ratios(cfg, st["nnz"], L),
+            "diff_density": diff_density(cfg, rr.store_t["rowptr"].cpu().numpy(), st["master"], L),
             "restore_us_per_agent_layer": round(stage_ms["restore"] * 1e3 / (N * L), 4),
             "host_link": None if not args.store_on_host else {
                 "restore_reads_gbs": round((2 * L * cfg.n_shared * cfg.elems * 2 + st["nnz"] *

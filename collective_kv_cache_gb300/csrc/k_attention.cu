@@ -12,9 +12,9 @@
 // Work unit = (layer, kv head, agent, 512 positions of the agent's context), one warp:
 //   - each position's K and V rows of the head (D bf16 each) are staged in shared memory
 //     by cp.async.bulk, 16 positions a stage, on a ring of two stages with mbarriers (two
-//     stages keep the shared memory at 17 KB a warp, so twelve warps fit on an SM).
-//     Every wait is bounded: on time-out the unit records TD_ERR_DEVICE_TIMEOUT, waits
-//     (bounded again) for the copies it issued and returns;
+//     stages keep the shared memory at 18 KB a warp, so twelve warps fit on an SM). Every
+//     wait is bounded in time (0.2 s by the global timer); on time-out the unit records
+//     TD_ERR_DEVICE_TIMEOUT, waits (bounded again) for the copies it issued and returns;
 //   - both products on the tensor cores, mma.sync m16n8k16 bf16 with float32 accumulators,
 //     the head group's G <= 8 query heads as rows (rows G..15 zero). A turned query is
 //     float32: it is split into a bf16 high part and a bf16 low part, two products per
@@ -34,7 +34,7 @@ namespace td {
 
 namespace {
 
-constexpr unsigned kSpinLimit = 1u << 20;   // mbarrier polls before a unit gives up
+constexpr uint64_t kWaitLimitNs = 200000000ull;   // 0.2 s: a healthy stage lands in microseconds
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -63,8 +63,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the phase with the given parity, for at most kWaitLimitNs of wall time.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
-  for (unsigned it = 0; it < kSpinLimit; ++it)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (global_ns() - t0 < kWaitLimitNs)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -185,7 +194,7 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
   auto fire = [&](int k, const uint16_t* src) {
     const unsigned ok = __ballot_sync(0xFFFFFFFFu, src != nullptr);
     uint64_t* bar = &s_bar[k % kAttnDepth];
-    if (lane == 0) mbar_arrive_expect_tx(bar, __popc(ok) * (D * 2));
+    if (lane == 0) mbar_arrive_expect_tx(bar, __popc(ok) * (D * 2) + A.tx_pad);
     __syncwarp();
     if (src)
       bulk_g2s(((lane >> 4) ? s_v : s_k)[k % kAttnDepth] + (lane & 15) * RS, src, D * 2, bar);

@@ -53,6 +53,7 @@ struct td_ctx {
   uint32_t* d_err = nullptr;
   float* d_attn = nullptr;          // attention partials, grown on demand
   size_t attn_cap = 0;              // its size in floats
+  uint32_t attn_tx_pad = 0;         // fault injection: bytes the attention never receives
   // pinned host words for results
   int64_t* h_words = nullptr;       // [4]
 };
@@ -282,6 +283,7 @@ td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store
   a.nl = layer_end - layer_begin;
   a.layer_begin = layer_begin;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.tx_pad = c->attn_tx_pad;
   a.err = c->d_err;
   // partials of the largest launch; grown once, after the work that used them
   auto units_of = [&](int x) {
@@ -721,6 +723,12 @@ td_status td_paged_attention(td_ctx* c, const td_round* r, const td_paged* pool,
                              float* out, float* lse, void* stream) {
   return run_attention(c, r, nullptr, pool, agents, n_list, layer_begin, layer_end, q, n_q_heads,
                        scale, out, lse, stream);
+}
+
+td_status td_inject_attention_wait_fault(td_ctx* c, uint32_t bytes) {
+  if (!c) return TD_ERR_INVALID_ARG;
+  c->attn_tx_pad = bytes;
+  return TD_OK;
 }
 
 td_status td_get_error(td_ctx* c, void* stream, uint32_t* bits_out) {

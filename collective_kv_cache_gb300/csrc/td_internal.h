@@ -155,6 +155,7 @@ struct AttnArgs {
   int nq, G;                 // query heads, query heads per kv head
   int nl, layer_begin, sl0;  // layers; store layer of layer_begin
   float scale_log2;          // softmax scale * log2(e)
+  uint32_t tx_pad;           // extra bytes every stage expects (fault injection; 0 normally)
   uint32_t* err;
 };
 

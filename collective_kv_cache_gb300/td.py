@@ -93,6 +93,7 @@ def _load() -> C.CDLL:
                                VP, I32, C.c_float, VP, VP, VP],
         "td_paged_attention": [VP, P(td_round), P(td_paged), VP, I32, I32, I32, VP, I32,
                                C.c_float, VP, VP, VP],
+        "td_inject_attention_wait_fault": [VP, C.c_uint32],
         "td_form_rounds": [P(td_prompt), I32, I32, I32, VP, I32, VP, VP, P(I32)],
         "td_group_round": [P(td_prompt), I32, I32, VP, I32, I32, I32, VP, P(I32), VP, P(I32),
                            VP, VP],
@@ -114,7 +115,7 @@ EXPORTS = ("td_ctx_create", "td_ctx_destroy", "td_status_string", "td_round_offs
            "td_fused_restore", "td_get_error", "td_check_select_noalloc",
            "td_check_select_group", "td_pick_master_min_deviation", "td_segment_hash",
            "td_form_rounds", "td_group_round", "td_materialise_mirror",
-           "td_fused_attention", "td_paged_attention")
+           "td_fused_attention", "td_paged_attention", "td_inject_attention_wait_fault")
 
 
 def lib_path() -> str:
@@ -238,6 +239,11 @@ def td_paged_attention(ctx, rnd, pool, agents, layer_begin, layer_end, q, n_q_he
                                 ag.ctypes.data if ag.size else None, ag.size, layer_begin,
                                 layer_end, q, n_q_heads, scale, out, lse, stream)
     return _check(s, "td_paged_attention") if check else s
+
+
+def td_inject_attention_wait_fault(ctx, nbytes: int) -> int:
+    return _check(_lib.td_inject_attention_wait_fault(ctx, nbytes),
+                  "td_inject_attention_wait_fault")
 
 
 def td_materialise_mirror(ctx, rnd, store, agent, layer_begin, layer_end, dense_k, dense_v,

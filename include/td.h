@@ -367,6 +367,14 @@ td_status td_group_round(const td_prompt* prompts, int32_t n_prompts, int32_t se
                          int32_t* block_len, int32_t* n_blocks, int32_t* hist_len,
                          int32_t* perm);
 
+/* Fault injection for tests; no counterpart in the paper. With bytes > 0 every later
+ * td_fused_attention / td_paged_attention call on this context makes each stage's barrier
+ * expect `bytes` more than its copies deliver, so every bounded wait runs out (0.2 s of
+ * device time each): the units record TD_ERR_DEVICE_TIMEOUT in the error word, wait
+ * (bounded) for their own copies and return, and the outputs are not valid. No copy is
+ * lost and nothing faults: the context stays usable. bytes = 0 restores normal calls. */
+td_status td_inject_attention_wait_fault(td_ctx* ctx, uint32_t bytes);
+
 /* Synchronize the stream, read and clear the error word. Returns TD_OK when no device
  * fault was recorded, else the lowest td_status code recorded; bits_out (HOST, or NULL)
  * receives the whole word (bit c set = code c recorded). */

@@ -120,3 +120,11 @@ def test_storage_ratios_match_the_oracle_closed_form():
     r = bench.storage_ratios(cfg, nnz, cfg.n_layers)
     assert abs(r["round_ratio"] - orc.round_ratio(cfg, nnz)) < 1e-3
     assert abs(r["per_mirror_ratio"] - orc.mirror_ratio(cfg, nnz // (cfg.n_agents - 1))) < 0.05
+
+
+def test_diff_density_from_row_pointers():
+    cfg = synth.tiny()        # 3 agents, 2 layers, 96 shared tokens -> 6 blocks per layer
+    rowptr = np.cumsum([0, 2, 3, 0, 0, 1, 4])        # rows: (a0 l0) (a0 l1) (a1 l0) ...
+    d = bench.diff_density(cfg, rowptr, master=1, nl=2)
+    assert d["blocks_per_layer"] == 6 and d["max"] == 4
+    assert d["mean"] == 2.5 and d["changed_fraction"] == round(2.5 / 6, 4)

@@ -231,3 +231,42 @@ def test_fused_attention_rejects_bad_arguments():
     # no agents: nothing to do
     td.td_fused_attention(rr.ctx.handle, rr.round, rr.store, rr.pool, [], 0, cfg.n_layers,
                           q.data_ptr(), 6, 0.1, out.data_ptr(), None, rr.s)
+
+
+def test_wait_timeout_is_reported_and_the_context_recovers():
+    """Fault injection on the host (td_inject_attention_wait_fault): every stage's barrier
+    expects bytes that never come, each bounded wait runs out, the error word says
+    TD_ERR_DEVICE_TIMEOUT and nothing faults; the next call on the same context is right."""
+    from collective_kv_cache_gb300 import runner as R
+    from collective_kv_cache_gb300 import td
+    cfg, nq = _mini(n_agents=2, n_layers=1, check_layer=0, seed=112), 6
+    orc = oracle.get()
+    ch = rk.run_oracle_chain(rk.make_inputs(cfg, map_history=True), restore=False)
+    rnd = ch.rnd
+    pool = oracle.new_pool(cfg, rnd.num_pages)
+    rk.fill_history(cfg, rnd, pool)
+    agents = list(range(cfg.n_agents))
+    q = synth.decode_queries(cfg, nq, agents, 0, 1)
+    st, out_o, _ = orc.attention(cfg, ch.desc, ch.master, ch.store, agents, pool, rnd.num_pages,
+                                 rnd.block_table, q, nq, 0.125)
+    assert st == 0
+    dev = torch.device("cuda")
+    rr = R.RoundRunner(cfg, rnd.block_len, rnd.hist_len, rnd.perm, rnd.block_table, rnd.num_pages)
+    rr.pool_t.copy_(R.to_device_bf16(pool, dev).reshape(rr.pool_t.shape))
+    _, store = _store_tensors(cfg, ch.store, dev)
+    qd = R.to_device_bf16(q, dev)
+    out = torch.zeros(q.shape, dtype=torch.float32, device=dev)
+
+    def call():
+        td.td_fused_attention(rr.ctx.handle, rr.round, store, rr.pool, agents, 0, 1,
+                              qd.data_ptr(), nq, 0.125, out.data_ptr(), None, rr.s)
+
+    td.td_inject_attention_wait_fault(rr.ctx.handle, 16)
+    call()
+    s, bits = rr.get_error()
+    assert s == td.TD_ERR_DEVICE_TIMEOUT and bits == (1 << td.TD_ERR_DEVICE_TIMEOUT), (s, bits)
+    td.td_inject_attention_wait_fault(rr.ctx.handle, 0)
+    call()
+    s, bits = rr.get_error()
+    assert s == 0 and bits == 0
+    assert np.abs(out.cpu().numpy() - out_o).max() < 5e-3
