@@ -17,10 +17,9 @@
 //           diff blocks (a 32-token block is two tiles): reads its canonical data
 //           once, builds the Master's (recomputed K turned back by R(-off)) and writes it,
 //           then for each candidate Mirror builds its data, writes it at its candidate
-//           place and notes in shared memory whether it differs (one warp vote); after
-//           the candidates, one thread per differing candidate ORs the block's flag,
-//           without waiting for the result. One CTA per block writes the slot map and
-//           block indices of the common case (every candidate kept);
+//           place and, where it differs (one warp vote), ORs the block's flag without
+//           waiting for the result. One CTA per block writes the slot map and block
+//           indices of the common case (every candidate kept);
 //   rows    one CTA: each (agent, layer) row's record count from its flags, one warp a
 //           row, then their prefix sum -> rowptr, and whether the fix-up must run;
 //   fixup   only when some candidate equalled the Master's block: compacts the slot map
@@ -338,7 +337,6 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
   __shared__ unsigned s_bits[kAgentChunk];
   __shared__ int s_first[kAgentChunk];
   __shared__ int s_list[kAgentChunk];        // the chunk's candidates, in agent order
-  __shared__ unsigned s_diff[kAgentChunk];   // candidate j of the list differs somewhere
   __shared__ int s_nc;
   extern __shared__ uint4 s_stage[];         // [kStageDepth][2][kItems][blockDim]
   const int slot_cells = 2 * kItems * blockDim.x;
@@ -365,7 +363,6 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
         s_place[x] = place;
         s_bits[x] = ibits;
         s_first[x] = ibits ? fr : 0;
-        s_diff[x] = 0u;
         if (designated && !over) {   // slot map and index of the common case
           a.store.slot[(static_cast<int64_t>(i) * a.nl + li) * nb + b] =
               static_cast<int32_t>(place);
@@ -423,17 +420,11 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
           store_item<kItems>(a, kv, rec, h, r, z, z);
         }
       }
-      if (__any_sync(0xFFFFFFFFu, d) && lane == 0) s_diff[j] = 1u;   // same value from all
+      // a warp whose rows differ ORs the block's flag, without waiting for the result
+      if (__any_sync(0xFFFFFFFFu, d) && lane == 0)
+        atomicOr(a.sc.flag + (static_cast<int64_t>(i) * a.nl + li) * nb + b, 1u);
     }
     cp_async_wait<0>();
-    // the chunk's verdicts: one global flag per candidate that differs, set in parallel
-    // and without waiting for the result (the other half-tile may set it too)
-    __syncthreads();
-    for (int j = threadIdx.x; j < nc; j += blockDim.x) {
-      if (!s_diff[j]) continue;
-      const int i = c0 + s_list[j];
-      atomicOr(a.sc.flag + (static_cast<int64_t>(i) * a.nl + li) * nb + b, 1u);
-    }
   }
 }
 
