@@ -249,6 +249,18 @@ td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store
     if (layer_begin < store->layer_begin || layer_end > store->layer_end ||
         store->layer_begin < 0 || store->layer_end > c->shape.n_layers)
       return TD_ERR_INVALID_ARG;
+    // the rows are staged by the bulk-copy engine from device memory only
+    const void* ptrs[] = {store->master_k, store->master_v, store->slot, store->val_k,
+                          store->val_v};
+    for (const void* p : ptrs) {
+      if (!p) continue;
+      cudaPointerAttributes at;
+      if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return TD_ERR_INVALID_ARG;
+      }
+      if (at.type != cudaMemoryTypeDevice) return TD_ERR_INVALID_ARG;
+    }
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   td_status s = prepare_round(c, r, st);

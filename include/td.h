@@ -284,8 +284,9 @@ td_status td_check_select_noalloc(const td_shape* shape, const td_round* round,
  *             at the query's position), 4-byte aligned
  *   out       DEVICE float [layer_end-layer_begin][n_list][n_q_heads][D]
  *   lse       DEVICE float [layer_end-layer_begin][n_list][n_q_heads], or NULL
- * Head dims 64 and 128 (else TD_ERR_INVALID_ARG). The context owns the partial results'
- * scratch and grows it when a call needs more (synchronising the stream first). An
+ * Head dims 64 and 128 (else TD_ERR_INVALID_ARG). The store must be in device memory (a
+ * store kept in host memory is refused with TD_ERR_INVALID_ARG: restore from it instead).
+ * The context owns the partial results' scratch and grows it when a call needs more (synchronising the stream first). An
  * unmapped history page sets TD_ERR_UNMAPPED_PAGE in the error word; a bounded wait on the
  * copy engine that runs out sets TD_ERR_DEVICE_TIMEOUT (that unit's result is not written). */
 td_status td_fused_attention(td_ctx* ctx, const td_round* round, const td_diff_store* store,

@@ -270,3 +270,19 @@ def test_wait_timeout_is_reported_and_the_context_recovers():
     s, bits = rr.get_error()
     assert s == 0 and bits == 0
     assert np.abs(out.cpu().numpy() - out_o).max() < 5e-3
+
+
+def test_fused_attention_refuses_a_store_in_host_memory():
+    from collective_kv_cache_gb300 import runner as R
+    from collective_kv_cache_gb300 import td
+    import bench
+    cfg = _mini(seed=113)
+    rnd = synth.make_round(cfg, map_history=True)
+    rr = R.RoundRunner(cfg, rnd.block_len, rnd.hist_len, rnd.perm, rnd.block_table, rnd.num_pages)
+    bench.host_store(rr, 8)
+    rr.store.layer_begin, rr.store.layer_end = 0, cfg.n_layers
+    q = torch.zeros((cfg.n_layers, 1, 6, cfg.head_dim), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(q.shape, dtype=torch.float32, device="cuda")
+    with pytest.raises(td.TDError):
+        td.td_fused_attention(rr.ctx.handle, rr.round, rr.store, rr.pool, [0], 0, cfg.n_layers,
+                              q.data_ptr(), 6, 0.1, out.data_ptr(), None, rr.s)
