@@ -286,3 +286,53 @@ def test_fused_attention_refuses_a_store_in_host_memory():
     with pytest.raises(td.TDError):
         td.td_fused_attention(rr.ctx.handle, rr.round, rr.store, rr.pool, [0], 0, cfg.n_layers,
                               q.data_ptr(), 6, 0.1, out.data_ptr(), None, rr.s)
+
+
+def test_three_hundred_agents_span_two_launches():
+    """More agents than one launch carries (256): restore and both attentions split the
+    list; every agent's rows must still be right, the second launch's included."""
+    from collective_kv_cache_gb300 import runner as R
+    from collective_kv_cache_gb300 import td
+    cfg = _mini(n_agents=300, n_layers=1, check_layer=0, block_lens=(20, 13), hist_range=(0, 20),
+                seed=114)
+    nq = 4
+    orc = oracle.get()
+    ch = rk.run_oracle_chain(rk.make_inputs(cfg, map_history=True), restore=False)
+    rnd = ch.rnd
+    pool = oracle.new_pool(cfg, rnd.num_pages)
+    rk.fill_history(cfg, rnd, pool)
+    agents = list(range(cfg.n_agents))[::-1]            # reversed, so list order matters
+    q = synth.decode_queries(cfg, nq, agents, 0, 1)
+    st, out_o, lse_o = orc.attention(cfg, ch.desc, ch.master, ch.store, agents, pool,
+                                     rnd.num_pages, rnd.block_table, q, nq, 0.125)
+    assert st == 0
+    dev = torch.device("cuda")
+    rr = R.RoundRunner(cfg, rnd.block_len, rnd.hist_len, rnd.perm, rnd.block_table, rnd.num_pages)
+    rr.pool_t.copy_(R.to_device_bf16(pool, dev).reshape(rr.pool_t.shape))
+    t, store = _store_tensors(cfg, ch.store, dev)
+    qd = R.to_device_bf16(q, dev)
+    out = torch.zeros(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.zeros(q.shape[:-1], dtype=torch.float32, device=dev)
+    td.td_fused_attention(rr.ctx.handle, rr.round, store, rr.pool, agents, 0, 1, qd.data_ptr(),
+                          nq, 0.125, out.data_ptr(), lse.data_ptr(), rr.s)
+    torch.cuda.synchronize()
+    assert rr.get_error()[0] == 0
+    assert np.abs(out.cpu().numpy() - out_o).max() < 5e-3
+    assert np.abs(lse.cpu().numpy() - lse_o).max() < 5e-3
+    # the restore over the same 300 agents, bit for bit, then attention over the pages
+    pool_r = pool.copy()
+    assert orc.fused_restore(cfg, ch.desc, ch.master, ch.store, np.asarray(agents), pool_r,
+                             rnd.num_pages, rnd.block_table, frame=0) == 0
+    rr.store = store
+    store.layer_begin, store.layer_end = 0, 1
+    rr.fused_restore(agents)
+    torch.cuda.synchronize()
+    assert np.array_equal(R.bits_of(rr.pool_t), pool_r)
+    st, out_p, _ = orc.attention(cfg, ch.desc, ch.master, ch.store, agents, pool_r,
+                                 rnd.num_pages, rnd.block_table, q, nq, 0.125, from_pool=True)
+    assert st == 0
+    td.td_paged_attention(rr.ctx.handle, rr.round, rr.pool, agents, 0, 1, qd.data_ptr(), nq,
+                          0.125, out.data_ptr(), None, rr.s)
+    torch.cuda.synchronize()
+    assert rr.get_error()[0] == 0
+    assert np.abs(out.cpu().numpy() - out_p).max() < 5e-3
