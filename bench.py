@@ -662,7 +662,14 @@ def bench_attention(cfg, seed, device, reps=10):
 
 
 def report_chunked(args, cfg, seed, device, rank, world):
+    local = device.index if device.index is not None else 0
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] \
+        if world == 1 else str(local)
+    clk = ClockSampler(gpu_id if gpu_id.isdigit() else "0").__enter__()
+    clk.mark("load_start")
     stage_ms, k, nnz, master = bench_chunked(args, cfg, seed, device)
+    clk.mark("load_end")
+    clk.__exit__(None, None, None)
     N, L = cfg.n_agents, cfg.n_layers
     ms = sum(stage_ms.values())
     ms_max = reduce_max(ms, device)
@@ -694,7 +701,9 @@ def report_chunked(args, cfg, seed, device, rank, world):
                          "peak": peak, "unit": "GB/s",
                          "frac": round(by[dom] / (stage_ms[dom] * 1e-3) / 1e9 / peak, 4),
                          "traffic": None, "peak_kind": peak_kind},
-            "gpu_launches": args.steps * (4 + 4 * ((L + args.chunk_layers - 1) // args.chunk_layers)),
+            "storage": storage_ratios(cfg, nnz, L),
+            "gpu_launches": args.steps * (4 + 5 * ((L + args.chunk_layers - 1) // args.chunk_layers)),
+            "clocks": clk.summary(),
             "e2e": None, "cpu_baseline": None,
         }
         print(json.dumps(line), flush=True)
