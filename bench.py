@@ -118,6 +118,31 @@ def diff_density(cfg, rowptr, master: int, nl: int) -> dict:
             "max": int(mir.max()), "changed_fraction": round(float(mir.mean()) / nb, 4)}
 
 
+def round_formation(cfg, rnd, reps: int = 5) -> dict:
+    """Host cost of building this round from its agents' token prompts (segment hashing,
+    grouping, the round descriptor), and a check that the descriptor is the round's."""
+    from collective_kv_cache_gb300 import synth, td
+    sep = 151643
+    prompts = synth.round_prompts(rnd, sep)
+    pages = [rnd.block_table[i] for i in range(cfg.n_agents)]
+    t_form = t_group = 0.0
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        g, st, n = td.td_form_rounds(prompts, sep, cfg.page_size, pages=pages)
+        t1 = time.perf_counter()
+        members, block_len, hist_len, perm = td.td_group_round(prompts, sep, g, 0)
+        t2 = time.perf_counter()
+        t_form += t1 - t0
+        t_group += t2 - t1
+    first = rnd.perm[0]
+    same = (n == 1 and not st.any() and np.array_equal(block_len, rnd.block_len[first]) and
+            np.array_equal(hist_len, rnd.hist_len) and np.array_equal(first[perm], rnd.perm))
+    return {"prompt_tokens": int(sum(len(p) for p in prompts)),
+            "form_rounds_ms": round(t_form / reps * 1e3, 3),
+            "group_round_ms": round(t_group / reps * 1e3, 3),
+            "descriptor_matches_round": bool(same)}
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -389,6 +414,7 @@ def bench_ours(args, rank, world, local_rank):
     if args.store_on_host:
         cfg = cfg.replace(name=cfg.name + "_store_in_host_memory")
     st = setup_round(cfg, seed, device, store_on_host=args.store_on_host)
+    formation = round_formation(cfg, st["rnd"]) if rank == 0 else None
     rr = st["rr"]
     agents = list(range(cfg.n_agents))
     N, L = cfg.n_agents, cfg.n_layers
@@ -498,6 +524,7 @@ def bench_ours(args, rank, world, local_rank):
             "stages": {n: {"ms": round(stage_ms[n], 5), "bytes": by[n],
                            "gbs": round(by[n] / (stage_ms[n] * 1e-3) / 1e9, 1)} for n in STAGES},
             "diff_blocks": st["nnz"], "selected_per_agent": st["k"], "master": st["master"],
+            "round_formation": formation,
             "storage": storage_ratios(cfg, st["nnz"], L),
             "diff_density": diff_density(cfg, rr.store_t["rowptr"].cpu().numpy(), st["master"], L),
             "restore_us_per_agent_layer": round(stage_ms["restore"] * 1e3 / (N * L), 4),

@@ -136,8 +136,9 @@ td_status td_form_rounds(const td_prompt* prompts, int32_t n_prompts, int32_t se
       continue;
     }
     std::unordered_set<int32_t> used;
-    if (p.pages)
-      for (int64_t pos = hist; pos < hist + span; ++pos) used.insert(p.pages[pos / page_size]);
+    if (p.pages && span > 0)   // the pages holding positions [hist, hist + span)
+      for (int64_t lp = hist / page_size; lp <= (hist + span - 1) / page_size; ++lp)
+        used.insert(p.pages[lp]);
     int32_t target = -1;
     auto& cands = open[key];
     for (int32_t gi : cands) {

@@ -168,6 +168,30 @@ def decode_queries(cfg: "RoundConfig", n_q_heads: int, agents, layer_begin: int,
     return out
 
 
+def round_prompts(rnd: "Round", sep: int, vocab: int = 150000, seed=None):
+    """Token prompts of a round: agent i's history (hist_len[i] tokens), then the shared
+    blocks in its order, each block starting with the separator `sep` followed by its
+    block_len - 1 content tokens (the same for every agent). Tokens in [1, vocab), never
+    `sep`. Returns a list of int32 arrays."""
+    cfg = rnd.cfg
+    seed = cfg.seed if seed is None else seed
+
+    def toks(key, n):
+        t = randint(key, np.arange(n), 1, vocab - 2).astype(np.int32)
+        return np.where(t >= sep, t + 1, t).astype(np.int32)
+
+    blocks = []
+    for j, L in enumerate(rnd.block_len):
+        body = toks(stream_key(seed, "block-tokens", j), int(L) - 1)
+        blocks.append(np.concatenate([np.array([sep], np.int32), body]))
+    out = []
+    for i, h in enumerate(rnd.hist_len):
+        parts = [toks(stream_key(seed, "hist-tokens", i), int(h))]
+        parts += [blocks[j] for j in rnd.perm[i]]
+        out.append(np.concatenate(parts).astype(np.int32))
+    return out
+
+
 def randint(key, counters, lo: int, hi: int) -> np.ndarray:
     """Integers uniform on [lo, hi] (inclusive)."""
     span = _U(hi - lo + 1)

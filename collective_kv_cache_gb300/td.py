@@ -292,7 +292,8 @@ def td_group_round(prompts, sep_token, group_of, group, cap_members=None, cap_bl
     arr, keep = _prompts(prompts)
     n = len(prompts)
     cm = cap_members or max(n, 1)
-    cb = cap_blocks or max(max((sum(1 for t in p if t == sep_token) for p in prompts), default=1), 1)
+    cb = cap_blocks or max(max((int(np.count_nonzero(np.asarray(p) == sep_token))
+                                for p in prompts), default=1), 1)
     go = np.ascontiguousarray(np.asarray(group_of, dtype=np.int32))
     mem = np.zeros(cm, np.int32)
     bl = np.zeros(cb, np.int32)

@@ -128,3 +128,13 @@ def test_diff_density_from_row_pointers():
     d = bench.diff_density(cfg, rowptr, master=1, nl=2)
     assert d["blocks_per_layer"] == 6 and d["max"] == 4
     assert d["mean"] == 2.5 and d["changed_fraction"] == round(2.5 / 6, 4)
+
+
+def test_round_formation_gives_back_the_round():
+    from collective_kv_cache_gb300 import build
+    build.build()
+    cfg = synth.qwen7b()
+    rnd = synth.make_round(cfg)
+    r = bench.round_formation(cfg, rnd, reps=1)
+    assert r["descriptor_matches_round"]
+    assert r["prompt_tokens"] == int(rnd.hist_len.sum()) + cfg.n_agents * cfg.n_shared
