@@ -37,7 +37,7 @@ LAUNCHES_PER_STEP = 9    # rerotate 1, deviation + top-k 2, master 1, encode 4, 
 # DRAM bytes (read + write) per launch of the roofline kernels at the benchmarked size, from
 # one ncu capture of these kernels as they are now (dram__bytes_read.sum +
 # dram__bytes_write.sum); set an entry to None when its kernel changes.
-MEASURED_TRAFFIC = {"qwen7b": {"restore": 2320700000, "rerotate": 1551100000}}
+MEASURED_TRAFFIC = {"qwen7b": {"restore": 2320800000, "rerotate": 1550900000}}
 CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
