@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 
 METRIC = "restore+reuse KV GB/s (% of GB300 HBM peak); agent-rounds/sec, 7B shape"
 UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal (the measured copy peak is the roofline)
 LAUNCHES_PER_STEP = 9    # rerotate 1, deviation + top-k 2, master 1, encode 4, restore 1
 # DRAM bytes (read + write) per launch of the roofline kernels at the benchmarked size, from
 # one ncu capture of these kernels as they are now (dram__bytes_read.sum +
@@ -521,6 +522,7 @@ def bench_ours(args, rank, world, local_rank):
                        "l2": "inputs larger than L2 (step moves %.2f GB); no flush" % (step_bytes / 1e9)},
             "agent_rounds_per_s": round(agent_rounds, 1),
             "hbm_frac_of_peak": round(value / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
+            "hbm_frac_of_nominal": round(value / NOMINAL_HBM_GBS, 4),
             "stages": {n: {"ms": round(stage_ms[n], 5), "bytes": by[n],
                            "gbs": round(by[n] / (stage_ms[n] * 1e-3) / 1e9, 1)} for n in STAGES},
             "diff_blocks": st["nnz"], "selected_per_agent": st["k"], "master": st["master"],
