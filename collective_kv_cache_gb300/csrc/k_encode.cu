@@ -46,7 +46,6 @@ struct EncArgs {
   int32_t* over;        // bound exceeds capacity
   int64_t* bound;
   int* prep_done;       // CTAs of prep finished (self-resetting)
-  int* main_done;       // CTAs of main finished (self-resetting)
   uint32_t* err;
 };
 
@@ -562,7 +561,6 @@ cudaError_t launch_encode(const Geom& g, const RoundDev& rd, const int32_t* mast
   a.m_ok = sc.need_fixup + 1;   // the context lays these ints out after need_fixup
   a.over = sc.need_fixup + 2;
   a.prep_done = sc.need_fixup + 3;
-  a.main_done = sc.need_fixup + 4;
   a.bound = bound_dev;
   a.err = err;
   if (nl <= 0) return cudaSuccess;
