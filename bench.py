@@ -488,6 +488,7 @@ def bench_ours(args, rank, world, local_rank):
 
     comparisons = None if args.no_compare else compare_baselines(st, agents, stage_ms, device)
     attention = None if args.no_attention else bench_attention(cfg, seed, device)
+    variants = None if args.no_compare else measure_variants(st, cfg, device)
 
     by = stage_bytes(cfg, N, L, st["k"], st["nnz"], N)
     step_bytes = sum(by.values())
@@ -550,6 +551,7 @@ def bench_ours(args, rank, world, local_rank):
             "clocks": clk.summary(),
             "comparisons": comparisons,
             "attention": attention,
+            "variants": variants,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -594,6 +596,54 @@ def compare_baselines(st, agents, stage_ms, device, reps=3):
             "fused_speedup": round(dense / stage_ms["restore"], 3),
             "what": "same round and kernels; serial = per-agent re-rotation + selection; "
                     "dense = materialise each agent's cache, then re-rotate it into pages"}
+
+
+def measure_variants(st, cfg, device, reps=10):
+    """The variant readings on the same round, after the timed region: the master with the
+    least total deviation of its selected tokens (A6) beside the default union-cost rule,
+    and one important set for the whole group (A8) beside the per-agent selection. CUDA
+    events on the launching stream, mean of `reps`. The default calls' outputs are put back
+    afterwards (the variants write the same selection and master buffers)."""
+    import torch
+    from collective_kv_cache_gb300 import td
+    rr = st["rr"]
+    k = rr.sel_t.shape[1]
+    sel_keep = rr.sel_t.clone()
+    master_keep = rr.master_t.clone()
+    score = torch.zeros(cfg.n_agents, dtype=torch.float64, device=device)
+    gdev = torch.zeros(cfg.n_shared, dtype=torch.float32, device=device)
+    sel_g = torch.zeros_like(rr.sel_t)
+
+    def timed(fn):
+        fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(rr.stream)
+        for _ in range(reps):
+            fn()
+        b.record(rr.stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    out = {
+        "pick_master_ms": timed(lambda: rr.pick_master(want_host=False)),
+        "pick_master_min_deviation_ms": timed(lambda: td.td_pick_master_min_deviation(
+            rr.ctx.handle, rr.round, rr.sel_t.data_ptr() if k else None, k, rr.dev_t.data_ptr(),
+            score.data_ptr(), rr.master_t.data_ptr(), rr.s, want_host=False)),
+        "check_select_ms": timed(lambda: rr.check_select(st["kf"])),
+        "check_select_group_ms": timed(lambda: td.td_check_select_group(
+            rr.ctx.handle, rr.round, cfg.check_layer, rr.pool, st["kf"].data_ptr(),
+            cfg.recompute_pct, sel_g.data_ptr() if k else None, rr.dev_t.data_ptr(),
+            gdev.data_ptr(), rr.s)),
+    }
+    rr.check_select(st["kf"])
+    rr.sel_t.copy_(sel_keep)
+    rr.master_t.copy_(master_keep)
+    torch.cuda.synchronize()
+    s, bits = rr.get_error()
+    if s != 0:
+        raise RuntimeError(f"device error word {bits:#x} in the variant readings")
+    return {n: round(v, 5) for n, v in out.items()}
 
 
 def attention_bytes(cfg, hist, nnz, n_q_heads, from_pool: bool) -> int:
