@@ -445,7 +445,9 @@ def bench_ours(args, rank, world, local_rank):
         main_stream = rr.stream
         rr.stream = torch.cuda.Stream(device)
         graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=rr.stream):
+        # thread-local capture: other threads (a process group's watchdog) keep their
+        # CUDA calls while this thread captures
+        with torch.cuda.graph(graph, stream=rr.stream, capture_error_mode="thread_local"):
             run_overlapped(st, agents, side, torch.cuda.Event(), torch.cuda.Event(), args)
         torch.cuda.synchronize()
         with torch.cuda.stream(rr.stream):
