@@ -78,14 +78,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
   return false;
 }
 
-// Global -> shared copy by the bulk-copy (TMA) engine; completion counted on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
-                                         uint64_t* bar) {
+// One box of a 2-D tensor map (16 rows x 64 bf16, 128-byte swizzle) into shared memory;
+// x = column (elements), y = row; completion counted on `bar`.
+__device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int x, int y,
+                                        uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+        "r"(smem_u32(bar))
       : "memory");
 }
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-swizzled box (rows of 128 bytes,
+// chunk c stored at c ^ (r mod 8); the box starts on a 1024-byte boundary).
+__device__ __forceinline__ int swz(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t* r, const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -117,11 +124,14 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
 
 template <int D, bool kFromPool>
 __global__ void __launch_bounds__(32, 12)
-attn_unit_kernel(AttnArgs A, AttnList list) {
+attn_unit_kernel(const __grid_constant__ AttnArgs A, const __grid_constant__ AttnList list,
+                 const __grid_constant__ AttnMaps maps) {
   constexpr int KCH = D / 16;         // k-chunks of one q.k product
-  constexpr int RS = D * 2 + 16;      // staged row stride in bytes (conflict-free ldmatrix)
-  __shared__ __align__(128) unsigned char s_k[kAttnDepth][kAttnStage * RS];
-  __shared__ __align__(128) unsigned char s_v[kAttnDepth][kAttnStage * RS];
+  constexpr int HALVES = D / 64;      // 64-column boxes per row (a box row is 128 bytes)
+  constexpr int BOX = kAttnStage * 128;               // one box: 16 rows x 128 bytes
+  constexpr int TILE = HALVES * BOX;                  // one stage of K (or V)
+  __shared__ __align__(1024) unsigned char s_k[kAttnDepth][TILE];
+  __shared__ __align__(1024) unsigned char s_v[kAttnDepth][TILE];
   __shared__ __align__(8) uint64_t s_bar[kAttnDepth];
   __shared__ float s_pt[kAttnStage][kAttnGMax + 1];   // softmax weights, transposed on the way
 
@@ -140,64 +150,77 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
     else hi = mid - 1;
   }
   const int x = lo, a = list.a[x];
-  const int S = A.rd.S, E = A.g.E;
+  const int S = A.rd.S, P = A.pool.P;
   const int n_ctx = list.hist[x] + S;
   const int hist = kFromPool ? n_ctx : list.hist[x];   // positions read from the pages
-  const int p0 = (c - list.base[x]) * kAttnChunk;
-  const int p1 = min(p0 + kAttnChunk, n_ctx);
+  // units of an agent: its history in 512-position chunks, then its shared tokens in
+  // 512-token chunks (so no unit straddles the two and every stage starts aligned)
+  const int nh = (hist + kAttnChunk - 1) / kAttnChunk;
+  const int cu = c - list.base[x];
+  const int p0 = cu < nh ? cu * kAttnChunk : hist + (cu - nh) * kAttnChunk;
+  const int p1 = cu < nh ? min(p0 + kAttnChunk, hist) : min(p0 + kAttnChunk, n_ctx);
   const int layer = A.layer_begin + li, sl = A.sl0 + li;
 
-  // rows past a partial stage are read by the products (with weight 0): keep them finite
-  for (int i = lane; i < kAttnDepth * kAttnStage * RS / 16; i += 32) {
-    reinterpret_cast<uint4*>(&s_k[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4*>(&s_v[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
   if (lane < kAttnDepth) mbar_init(&s_bar[lane], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncwarp();
 
-  // the stage that starts at position p: at most 16 positions of one segment (the history,
-  // or one shared block: the query's rotation is constant within a segment)
+  // the stage that starts at position p: at most 16 positions from one place, so one box
+  // holds them: within a page (history), or within a shared block and a diff block
   auto stage_end = [&](int p) {
-    int seg_end = hist;
-    if (p >= hist) {
-      const int j = __ldg(A.rd.tok_block + (p - hist));
-      seg_end = hist + (j + 1 < A.rd.M ? __ldg(A.rd.blk_start + j + 1) : S);
+    int e;
+    if (p < hist) {
+      e = min((p / P + 1) * P, hist);
+    } else {
+      const int t = p - hist;
+      const int j = __ldg(A.rd.tok_block + t);
+      const int blk_end = j + 1 < A.rd.M ? __ldg(A.rd.blk_start + j + 1) : S;
+      e = hist + min(blk_end, (t / A.rd.B + 1) * A.rd.B);
     }
-    return min(min(p + kAttnStage, seg_end), p1);
+    return min(min(p + kAttnStage, e), p1);
   };
   auto segment = [&](int p) { return p < hist ? -1 : __ldg(A.rd.tok_block + (p - hist)); };
 
-  // source row of this lane for the stage at p: lanes 0-15 the K rows, 16-31 the V rows
-  auto source = [&](int p, int n) -> const uint16_t* {
-    const int tk = lane & 15, kv = lane >> 4;
-    if (tk >= n) return nullptr;
-    const int pos = p + tk;
-    if (pos < hist) {
-      const int64_t row = pool_row_index(A.pool, a, layer, kv, pos, A.err);
-      return row >= 0 ? A.pool.base + row * E + h * D : nullptr;
-    }
-    const int t = pos - hist;
-    const int rec = __ldg(A.store.slot +
-                          (static_cast<int64_t>(a) * A.store.nl + sl) * A.rd.nb + t / A.rd.B);
-    if (rec >= A.store.capacity) {
-      atomicOr(A.err, err_bit(TD_ERR_INVALID_ARG));
-      return nullptr;
-    }
-    if (rec >= 0)
-      return (kv ? A.store.val_v : A.store.val_k) +
-             (static_cast<int64_t>(rec) * A.rd.B + t % A.rd.B) * E + h * D;
-    return (kv ? A.store.master_v : A.store.master_k) +
-           (static_cast<int64_t>(sl) * S + t) * E + h * D;
-  };
-  auto fire = [&](int k, const uint16_t* src) {
-    const unsigned ok = __ballot_sync(0xFFFFFFFFu, src != nullptr);
+  // lane 0 fires the stage at p: K and V boxes (HALVES each) from the page, the agent's
+  // record or the Master, all counted on the stage's barrier
+  auto fire = [&](int k, int p) {
+    if (lane != 0) return;
     uint64_t* bar = &s_bar[k % kAttnDepth];
-    if (lane == 0) mbar_arrive_expect_tx(bar, __popc(ok) * (D * 2) + A.tx_pad);
-    __syncwarp();
-    if (src)
-      bulk_g2s(((lane >> 4) ? s_v : s_k)[k % kAttnDepth] + (lane & 15) * RS, src, D * 2, bar);
+    const CUtensorMap* src_map = nullptr;
+    int row = 0;
+    bool pool_rows = false;
+    if (p < hist) {
+      const int64_t rk = pool_row_index(A.pool, a, layer, 0, p, A.err);
+      if (rk >= 0) {
+        src_map = &maps.pool;
+        row = static_cast<int>(rk);
+        pool_rows = true;
+      }
+    } else {
+      const int t = p - hist;
+      const int rec = __ldg(A.store.slot + (static_cast<int64_t>(a) * A.store.nl + sl) *
+                                               A.rd.nb + t / A.rd.B);
+      if (rec >= A.store.capacity) {
+        atomicOr(A.err, err_bit(TD_ERR_INVALID_ARG));
+      } else if (rec >= 0) {
+        src_map = &maps.val_k;
+        row = rec * A.rd.B + t % A.rd.B;
+      } else {
+        src_map = &maps.master_k;
+        row = sl * S + t;
+      }
+    }
+    mbar_arrive_expect_tx(bar, src_map ? 2u * TILE + A.tx_pad : A.tx_pad);
+    if (!src_map) return;
+    // the V rows: the pool's V half of the same page, or the V map of the same source
+    const CUtensorMap* v_map = pool_rows ? &maps.pool
+                             : (src_map == &maps.val_k ? &maps.val_v : &maps.master_v);
+    const int v_row = pool_rows ? row + static_cast<int>(A.pool.num_pages) * P : row;
+#pragma unroll
+    for (int hh = 0; hh < HALVES; ++hh) {
+      tma_box(s_k[k % kAttnDepth] + hh * BOX, src_map, h * D + hh * 64, row, bar);
+      tma_box(s_v[k % kAttnDepth] + hh * BOX, v_map, h * D + hh * 64, v_row, bar);
+    }
   };
 
   // this lane's query values: head gid of the group, dims kc*16 + tig*2 + {0, 1, 8, 9}
@@ -261,35 +284,38 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
   // prologue: the first stages in flight
   int ipos = p0, issued = 0;
   for (int k = 0; k < kAttnDepth && ipos < p1; ++k) {
-    const int e = stage_end(ipos);
-    fire(k, source(ipos, e - ipos));
-    ipos = e;
+    fire(k, ipos);
+    ipos = stage_end(ipos);
     ++issued;
   }
   int cseg = -2;
   int cpos = p0;
   bool failed = false;
-  // ldmatrix row addresses: K as the A operand (rows = positions), V transposed (rows = dims)
-  const int koff = (((lane >> 3) & 1) * 8 + (lane & 7)) * RS + (lane >> 4) * 16;
-  const int voff = ((lane >> 4) * 8 + (lane & 7)) * RS + ((lane >> 3) & 1) * 16;
+  // ldmatrix rows: K as the A operand (rows = positions), V transposed (rows = positions
+  // of the transposed tile); which 8x8 matrix this lane addresses
+  const int k_row = ((lane >> 3) & 1) * 8 + (lane & 7), k_c = lane >> 4;
+  const int v_row = (lane >> 4) * 8 + (lane & 7), v_c = (lane >> 3) & 1;
   for (int k = 0; cpos < p1; ++k) {
     const int cend = stage_end(cpos);
     const int n = cend - cpos;
     const int buf = k % kAttnDepth;
-    // the next stage's rows are looked up now, their copies fired after this stage
-    const bool more = ipos < p1;
-    int iend = ipos;
-    const uint16_t* nsrc = nullptr;
-    if (more) {
-      iend = stage_end(ipos);
-      nsrc = source(ipos, iend - ipos);
-    }
     if (!mbar_wait_bounded(&s_bar[buf], (k / kAttnDepth) & 1)) {
       failed = true;
       if (lane == 0) atomicOr(A.err, err_bit(TD_ERR_DEVICE_TIMEOUT));
       for (int k2 = k; k2 < issued; ++k2)   // the copies this unit issued, stage k's too
         mbar_wait_bounded(&s_bar[k2 % kAttnDepth], (k2 / kAttnDepth) & 1);
       break;
+    }
+    if (n < kAttnStage) {
+      // the boxes brought 16 rows; those past the stage get weight 0 below, and their V is
+      // cleared so that no stray value can reach the sums
+      for (int i = lane; i < (kAttnStage - n) * (TILE / kAttnStage / 16); i += 32) {
+        const int r = n + i / (TILE / kAttnStage / 16);
+        const int cc = i % (TILE / kAttnStage / 16);
+        *reinterpret_cast<uint4*>(s_v[buf] + (cc >> 3) * BOX + swz(r, cc & 7)) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
     }
     const int seg = segment(cpos);
     if (seg != cseg) {
@@ -301,11 +327,11 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
     float sacc[4][4];
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) sacc[ch][0] = sacc[ch][1] = sacc[ch][2] = sacc[ch][3] = 0.0f;
-    const unsigned char* kb = s_k[buf] + koff;
 #pragma unroll
     for (int kc = 0; kc < KCH; ++kc) {
       uint32_t af[4];
-      ldmatrix_x4(af, kb + kc * 32);
+      // chunk kc: box kc / 4, 16-byte chunks (kc % 4) * 2 + {0, 1} of the 128-byte row
+      ldmatrix_x4(af, s_k[buf] + (kc >> 2) * BOX + swz(k_row, (kc & 3) * 2 + k_c));
       mma_bf16_full(sacc[kc & 1], af, qhi[kc][0], qhi[kc][1]);
       if (two) mma_bf16_full(sacc[2 + (kc & 1)], af, qlo[kc][0], qlo[kc][1]);
     }
@@ -348,11 +374,10 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
     const uint32_t bh0 = pack_bf2(ph[0], ph[1]), bh1 = pack_bf2(ph[2], ph[3]);
     const uint32_t bl0 = pack_bf2(__fsub_rn(pt[0], ph[0]), __fsub_rn(pt[1], ph[1]));
     const uint32_t bl1 = pack_bf2(__fsub_rn(pt[2], ph[2]), __fsub_rn(pt[3], ph[3]));
-    const unsigned char* vb = s_v[buf] + voff;
 #pragma unroll
     for (int mt = 0; mt < KCH; ++mt) {
       uint32_t af[4];
-      ldmatrix_x4_trans(af, vb + mt * 32);
+      ldmatrix_x4_trans(af, s_v[buf] + (mt >> 2) * BOX + swz(v_row, (mt & 3) * 2 + v_c));
       oacc[mt][0] *= fac[0];
       oacc[mt][1] *= fac[1];
       oacc[mt][2] *= fac[0];
@@ -362,10 +387,11 @@ attn_unit_kernel(AttnArgs A, AttnList list) {
     }
     __syncwarp();   // this stage's buffers and s_pt are no longer read
     cpos = cend;
-    if (more) {
+    if (ipos < p1) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      fire(issued, nsrc);
-      ipos = iend;
+      fire(issued, ipos);
+      __syncwarp();
+      ipos = stage_end(ipos);
       ++issued;
     }
   }
@@ -432,10 +458,11 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs A, AttnList 
 }
 
 template <int D, bool kFromPool>
-static cudaError_t run_attn(const AttnArgs& a, const AttnList& list, cudaStream_t st) {
+static cudaError_t run_attn(const AttnArgs& a, const AttnList& list, const AttnMaps& maps,
+                            cudaStream_t st) {
   const int64_t units = static_cast<int64_t>(a.nl) * a.g.H * list.base[list.n];
   if (units == 0) return cudaSuccess;
-  attn_unit_kernel<D, kFromPool><<<static_cast<unsigned>(units), 32, 0, st>>>(a, list);
+  attn_unit_kernel<D, kFromPool><<<static_cast<unsigned>(units), 32, 0, st>>>(a, list, maps);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = static_cast<int64_t>(a.nl) * list.n * a.nq;
@@ -443,12 +470,14 @@ static cudaError_t run_attn(const AttnArgs& a, const AttnList& list, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_attention(const AttnArgs& a, const AttnList& list, bool from_pool,
-                             cudaStream_t st) {
+cudaError_t launch_attention(const AttnArgs& a, const AttnList& list, const AttnMaps& maps,
+                             bool from_pool, cudaStream_t st) {
   if (a.g.D == 128)
-    return from_pool ? run_attn<128, true>(a, list, st) : run_attn<128, false>(a, list, st);
+    return from_pool ? run_attn<128, true>(a, list, maps, st)
+                     : run_attn<128, false>(a, list, maps, st);
   if (a.g.D == 64)
-    return from_pool ? run_attn<64, true>(a, list, st) : run_attn<64, false>(a, list, st);
+    return from_pool ? run_attn<64, true>(a, list, maps, st)
+                     : run_attn<64, false>(a, list, maps, st);
   return cudaErrorInvalidValue;
 }
 

@@ -226,6 +226,39 @@ td_status pool_dev(const td_ctx* c, const td_round* r, const td_paged* p, PoolDe
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// cuTensorMapEncodeTiled from the driver, looked up once (no link-time dependency).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// A [rows][E] bf16 array as a 2-D tensor map with 16 x 64 boxes and 128-byte swizzle.
+bool row_map(CUtensorMap* m, const void* base, uint64_t rows, int E) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn || !base || rows == 0 || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(E), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(E) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kAttnStage)};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 // Decode attention of the listed agents: shared positions from the store (store != null)
 // or every position from the pages (store == null, the restored cache).
 td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store,
@@ -298,14 +331,37 @@ td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store
   a.tx_pad = c->attn_tx_pad;
   a.err = c->d_err;
   // partials of the largest launch; grown once, after the work that used them
-  auto units_of = [&](int x) {
-    return (static_cast<int64_t>(r->hist_len[agents[x]]) + c->S + kAttnChunk - 1) / kAttnChunk;
+  // an agent's units: its history, then its shared tokens, each in chunks of kAttnChunk
+  // (every position from the pages: the whole context in chunks)
+  auto units_of = [&](int x) -> int64_t {
+    const int64_t hl = r->hist_len[agents[x]];
+    if (!store) return (hl + c->S + kAttnChunk - 1) / kAttnChunk;
+    return (hl + kAttnChunk - 1) / kAttnChunk + (c->S + kAttnChunk - 1) / kAttnChunk;
   };
   int64_t most = 0;
   for (int x0 = 0; x0 < n_list; x0 += kMaxListAgents) {
     int64_t sum = 0;
     for (int x = x0; x < n_list && x < x0 + kMaxListAgents; ++x) sum += units_of(x);
     most = sum > most ? sum : most;
+  }
+  AttnMaps maps;
+  const uint64_t pool_rows = static_cast<uint64_t>(c->shape.n_layers) * 2 *
+                             static_cast<uint64_t>(pd.num_pages) * pd.P;
+  if (!row_map(&maps.pool, pd.base, pool_rows, c->g.E)) return TD_ERR_CUDA;
+  if (store) {
+    const uint64_t mrows = static_cast<uint64_t>(a.store.nl) * c->S;
+    const uint64_t vrows = static_cast<uint64_t>(store->capacity_blocks) * c->shape.diff_block;
+    if (!row_map(&maps.master_k, store->master_k, mrows, c->g.E) ||
+        !row_map(&maps.master_v, store->master_v, mrows, c->g.E))
+      return TD_ERR_CUDA;
+    const bool recs = vrows > 0 && store->val_k && store->val_v;
+    if (!row_map(&maps.val_k, recs ? store->val_k : store->master_k, recs ? vrows : mrows,
+                 c->g.E) ||
+        !row_map(&maps.val_v, recs ? store->val_v : store->master_v, recs ? vrows : mrows,
+                 c->g.E))
+      return TD_ERR_CUDA;
+  } else {
+    maps.master_k = maps.master_v = maps.val_k = maps.val_v = maps.pool;
   }
   const size_t need = static_cast<size_t>(most) * a.nl * H * kAttnGMax * (D + 2);
   if (need > c->attn_cap) {
@@ -332,7 +388,7 @@ td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store
     a.x0 = x0;
     a.part_o = c->d_attn;
     a.part_ml = c->d_attn + static_cast<size_t>(units) * kAttnGMax * D;
-    if (launch_attention(a, L, store == nullptr, st) != cudaSuccess) return TD_ERR_CUDA;
+    if (launch_attention(a, L, maps, store == nullptr, st) != cudaSuccess) return TD_ERR_CUDA;
   }
   return TD_OK;
 }

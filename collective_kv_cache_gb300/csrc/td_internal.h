@@ -1,6 +1,7 @@
 // td_internal.h - types shared by the host layer (td_host.cpp) and the kernels (*.cu).
 #pragma once
 
+#include <cuda.h>            // CUtensorMap: the attention kernels' tensor maps
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -159,8 +160,18 @@ struct AttnArgs {
   uint32_t* err;
 };
 
-cudaError_t launch_attention(const AttnArgs& a, const AttnList& list, bool from_pool,
-                             cudaStream_t st);
+// 2-D tensor maps ([rows][E] bf16, boxes of 16 rows x 64 columns, 128-byte swizzle) of the
+// places the attention kernels stage rows from.
+struct AttnMaps {
+  CUtensorMap pool;          // rows = [L][2][num_pages][P]
+  CUtensorMap master_k;      // rows = [nl][S]
+  CUtensorMap master_v;
+  CUtensorMap val_k;         // rows = [capacity][B]
+  CUtensorMap val_v;
+};
+
+cudaError_t launch_attention(const AttnArgs& a, const AttnList& list, const AttnMaps& maps,
+                             bool from_pool, cudaStream_t st);
 
 cudaError_t launch_materialise(const Geom& g, const RoundDev& rd, const StoreDev& store,
                                int agent, int sl0, int nl, uint16_t* dk, uint16_t* dv,
