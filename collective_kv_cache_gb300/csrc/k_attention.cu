@@ -10,9 +10,11 @@
 // once per block, q . R(off) X = (R(-off) q) . X, so shared rows are used as stored.
 //
 // Work unit = (layer, kv head, agent, 512 positions of the agent's context), one warp:
-//   - each position's K and V rows of the head (D bf16 each) are staged in shared memory
-//     by cp.async.bulk, 16 positions a stage, on a ring of two stages with mbarriers (two
-//     stages keep the shared memory at 18 KB a warp, so twelve warps fit on an SM). Every
+//   - the rows of the head (D bf16 per position) are staged in shared memory by the TMA
+//     engine from 2-D tensor maps of the pool, the records and the Master (16 x 64 boxes,
+//     128-byte swizzle): a stage is at most 16 positions from one page, one diff block and
+//     one shared block, so it arrives as D/64 boxes of K and D/64 of V. Two stages ring on
+//     mbarriers, 16 KB a warp, so thirteen warps fit on an SM. Every
 //     wait is bounded in time (0.2 s by the global timer); on time-out the unit records
 //     TD_ERR_DEVICE_TIMEOUT, waits (bounded again) for the copies it issued and returns;
 //   - both products on the tensor cores, mma.sync m16n8k16 bf16 with float32 accumulators,
@@ -123,7 +125,7 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
 }  // namespace
 
 template <int D, bool kFromPool>
-__global__ void __launch_bounds__(32, 12)
+__global__ void __launch_bounds__(32, 13)
 attn_unit_kernel(const __grid_constant__ AttnArgs A, const __grid_constant__ AttnList list,
                  const __grid_constant__ AttnMaps maps) {
   constexpr int KCH = D / 16;         // k-chunks of one q.k product
@@ -133,7 +135,6 @@ attn_unit_kernel(const __grid_constant__ AttnArgs A, const __grid_constant__ Att
   __shared__ __align__(1024) unsigned char s_k[kAttnDepth][TILE];
   __shared__ __align__(1024) unsigned char s_v[kAttnDepth][TILE];
   __shared__ __align__(8) uint64_t s_bar[kAttnDepth];
-  __shared__ float s_pt[kAttnStage][kAttnGMax + 1];   // softmax weights, transposed on the way
 
   const int lane = threadIdx.x;
   const int gid = lane >> 2, tig = lane & 3;   // mma fragment group / thread in group
@@ -359,7 +360,9 @@ attn_unit_kernel(const __grid_constant__ AttnArgs A, const __grid_constant__ Att
       m_run[c2] = m_new;
     }
     // P^T as the B operand of O^T += V^T P^T (k = positions, n = heads): transposed
-    // through shared memory, then split into two bf16 parts like the query
+    // through shared memory (the stage's K tile, read completely by now), then split into
+    // two bf16 parts like the query
+    float (*s_pt)[kAttnGMax + 1] = reinterpret_cast<float (*)[kAttnGMax + 1]>(s_k[buf]);
     s_pt[gid][2 * tig] = p[0];
     s_pt[gid][2 * tig + 1] = p[1];
     s_pt[gid + 8][2 * tig] = p[2];
