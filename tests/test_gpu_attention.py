@@ -53,6 +53,9 @@ CASES = {
     "mini_no_history": (_mini(hist_range=(0, 0), seed=107), 6),
     "mini_long_history": (_mini(hist_range=(700, 1500), seed=108), 6),   # several units each
     "mini_pct100": (_mini(recompute_pct=100, seed=109), 6),
+    # pages that do not hold a whole stage: a box reaches past the stage's page
+    "mini_p24": (_mini(page_size=24, hist_range=(30, 100), seed=115), 6),
+    "mini_p8_d128": (_mini(page_size=8, head_dim=128, hist_range=(30, 100), seed=116), 4),
     "qwen7b_2layers": (synth.qwen7b().replace(n_layers=2), 28),
 }
 
