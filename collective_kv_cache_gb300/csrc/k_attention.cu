@@ -436,23 +436,52 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs A, AttnList 
   const int x = static_cast<int>((w / A.nq) % list.n);
   const int li = static_cast<int>(w / (static_cast<int64_t>(A.nq) * list.n));
   const int h = gq / A.G, g = gq - h * A.G;
+  // the agent's units: contiguous from list.base[x] within (layer, kv head)
   const int total = list.base[list.n];
-  const int64_t u0 = (static_cast<int64_t>(li) * A.g.H + h) * total;
+  const int64_t u0 = (static_cast<int64_t>(li) * A.g.H + h) * total + list.base[x];
+  const int nu = list.base[x + 1] - list.base[x];
+  auto unit_of = [&](int i) { return u0 + i; };
+  // the units' maxima and sums a lane per unit (batches of 32), so that their loads are in
+  // flight together; then the weighted outputs, eight units' loads at a time
   float mx = -INFINITY;
-  for (int c = list.base[x]; c < list.base[x + 1]; ++c)
-    mx = fmaxf(mx, A.part_ml[((u0 + c) * kAttnGMax + g) * 2]);
+  for (int i0 = 0; i0 < nu; i0 += 32) {
+    const int i = i0 + lane;
+    if (i < nu) mx = fmaxf(mx, A.part_ml[(unit_of(i) * kAttnGMax + g) * 2]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   float l = 0.0f, acc[DPL];
 #pragma unroll
   for (int d = 0; d < DPL; ++d) acc[d] = 0.0f;
-  for (int c = list.base[x]; c < list.base[x + 1]; ++c) {
-    const int64_t unit = u0 + c;
-    const float m = A.part_ml[(unit * kAttnGMax + g) * 2];
-    const float wgt = m == -INFINITY ? 0.0f : exp2f(m - mx);
-    l = __fmaf_rn(A.part_ml[(unit * kAttnGMax + g) * 2 + 1], wgt, l);
-    const float* po = A.part_o + (unit * kAttnGMax + g) * D + lane * DPL;
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) acc[d] = __fmaf_rn(po[d], wgt, acc[d]);
+  for (int i0 = 0; i0 < nu; i0 += 32) {
+    const int i = i0 + lane;
+    float wgt = 0.0f;
+    if (i < nu) {
+      const int64_t unit = unit_of(i);
+      const float m = A.part_ml[(unit * kAttnGMax + g) * 2];
+      wgt = m == -INFINITY ? 0.0f : exp2f(m - mx);
+      l = __fmaf_rn(A.part_ml[(unit * kAttnGMax + g) * 2 + 1], wgt, l);
+    }
+    const int nb = min(32, nu - i0);
+#pragma unroll 8
+    for (int j = 0; j < nb; ++j) {
+      const float wj = __shfl_sync(0xFFFFFFFFu, wgt, j);
+      const float* po = A.part_o + (unit_of(i0 + j) * kAttnGMax + g) * D + lane * DPL;
+      if constexpr (DPL == 4) {
+        const float4 q4 = *reinterpret_cast<const float4*>(po);
+        acc[0] = __fmaf_rn(q4.x, wj, acc[0]);
+        acc[1] = __fmaf_rn(q4.y, wj, acc[1]);
+        acc[2] = __fmaf_rn(q4.z, wj, acc[2]);
+        acc[3] = __fmaf_rn(q4.w, wj, acc[3]);
+      } else {
+        const float2 q2 = *reinterpret_cast<const float2*>(po);
+        acc[0] = __fmaf_rn(q2.x, wj, acc[0]);
+        acc[1] = __fmaf_rn(q2.y, wj, acc[1]);
+      }
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
   const int64_t row = (static_cast<int64_t>(li) * A.n_list + A.x0 + x) * A.nq + gq;
   const float inv = 1.0f / l;
 #pragma unroll

@@ -300,11 +300,18 @@ __device__ __forceinline__ void staged_item(const EncArgs& a, int ag, int kv, un
   }
 }
 
+// 4- and 8-byte asynchronous copies (through L1), for the per-agent facts.
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(s), "l"(gmem) : "memory");
+}
+
 template <int kItems>
 __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_per_layer) {
-  const int m = *a.m_ok;
-  if (m < 0) return;
-  const int over = *a.over;
   const Unit un = unit_of(a.g, blockIdx.x, tiles_per_layer);
   const int kv = un.kv, li = un.li;
   const int t0 = un.b * kTile;
@@ -313,9 +320,33 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
   const int N = a.rd.N, nb = a.rd.nb, nbw = a.sc.nbw;
   const int lane = threadIdx.x & 31;
 
+  // the raw per-agent facts of this block for one chunk of agents, copied in by the first
+  // warp: the first chunk's copies leave at once and travel with the canonical rows
+  __shared__ unsigned s_word[kAgentChunk], s_sb[kAgentChunk];
+  __shared__ int s_fr[kAgentChunk], s_wp[kAgentChunk];
+  __shared__ int64_t s_ap[kAgentChunk + 1];
+  auto fetch_facts = [&](int c0, int n) {
+    for (int x = lane; x < n; x += 32) {
+      const int i = c0 + x;
+      cp_async4(&s_word[x], a.sc.cand + i * nbw + (b >> 5));
+      cp_async4(&s_sb[x], a.sc.selbits + static_cast<int64_t>(i) * nb + b);
+      cp_async4(&s_fr[x], a.sc.firstrank + static_cast<int64_t>(i) * nb + b);
+      cp_async4(&s_wp[x], a.sc.word_prefix + i * nbw + (b >> 5));
+      cp_async8(&s_ap[x], a.sc.agent_prefix + i);
+    }
+    if (lane == 0) cp_async8(&s_ap[n], a.sc.agent_prefix + c0 + n);
+    cp_async_commit();
+  };
+  if (threadIdx.x < 32) fetch_facts(0, min(kAgentChunk, N));
+
   HalfTile<kItems> h;
   load_half<kItems>(a, li, t0, tb0, kv, un.q0, h);
-
+  const int m = *a.m_ok;
+  if (m < 0) {
+    cp_async_wait<0>();
+    return;
+  }
+  const int over = *a.over;
   // the Master's half-tile, written dense
   const unsigned mbits = a.sc.selbits[static_cast<int64_t>(m) * nb + b];
   const int mfirst = mbits ? a.sc.firstrank[static_cast<int64_t>(m) * nb + b] : 0;
@@ -342,26 +373,28 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   for (int c0 = 0; c0 < N; c0 += kAgentChunk) {
     const int n = min(kAgentChunk, N - c0);
-    if (c0 > 0) __syncthreads();
+    if (c0 > 0) {
+      __syncthreads();
+      if (threadIdx.x < 32) fetch_facts(c0, n);
+    }
     if (threadIdx.x < 32) {
-      // the first warp alone: the chunk's per-agent facts (all loaded in one round trip;
-      // unused ones are ignored), then the candidates compacted in agent order
+      // the first warp alone: the chunk's candidate places, then the candidates compacted
+      // in agent order (no staging copy is pending here: the previous chunk drained them)
+      cp_async_wait<0>();
+      __syncwarp();
       for (int x = threadIdx.x; x < n; x += 32) {
         const int i = c0 + x;
-        const unsigned word = a.sc.cand[i * nbw + (b >> 5)];
-        const unsigned sb = a.sc.selbits[static_cast<int64_t>(i) * nb + b];
-        const int fr = a.sc.firstrank[static_cast<int64_t>(i) * nb + b];
-        const int64_t ap0 = a.sc.agent_prefix[i], ap1 = a.sc.agent_prefix[i + 1];
-        const int wp = a.sc.word_prefix[i * nbw + (b >> 5)];
+        const unsigned word = s_word[x];
+        const int64_t ap0 = s_ap[x], ap1 = s_ap[x + 1];
         const bool is_cand = (word >> (b & 31)) & 1u;
         const unsigned below = (b & 31) ? (word & ((1u << (b & 31)) - 1u)) : 0u;
         const int64_t place = is_cand ? ap0 * a.nl + static_cast<int64_t>(li) * (ap1 - ap0) +
-                                            wp + __popc(below)
+                                            s_wp[x] + __popc(below)
                                       : -1;
-        const unsigned ibits = is_cand ? sb : 0u;
+        const unsigned ibits = is_cand ? s_sb[x] : 0u;
         s_place[x] = place;
         s_bits[x] = ibits;
-        s_first[x] = ibits ? fr : 0;
+        s_first[x] = ibits ? s_fr[x] : 0;
         if (designated && !over) {   // slot map and index of the common case
           a.store.slot[(static_cast<int64_t>(i) * a.nl + li) * nb + b] =
               static_cast<int32_t>(place);
