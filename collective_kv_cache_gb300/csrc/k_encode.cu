@@ -20,8 +20,9 @@
 //           place and, where it differs (one warp vote), ORs the block's flag without
 //           waiting for the result. One CTA per block writes the slot map and block
 //           indices of the common case (every candidate kept);
-//   rows    one CTA: each (agent, layer) row's record count from its flags, one warp a
-//           row, then their prefix sum -> rowptr, and whether the fix-up must run;
+//   rows    each (agent, layer) row's record count from its flags, one warp a row over
+//           as many CTAs as the rows need; the CTA that finishes last (a self-resetting
+//           counter) takes their prefix sum -> rowptr and decides whether the fix-up runs;
 //   fixup   only when some candidate equalled the Master's block: compacts the slot map
 //           and indices and rewrites the kept blocks whose record moved (recomputed from
 //           the inputs, never copied); otherwise it returns at once.
@@ -46,8 +47,18 @@ struct EncArgs {
   int32_t* over;        // bound exceeds capacity
   int64_t* bound;
   int* prep_done;       // CTAs of prep finished (self-resetting)
+  int* rows_done;       // CTAs of the row count finished (self-resetting)
   uint32_t* err;
 };
+
+// Programmatic dependent launch within the encode: the next kernel of the stream may be
+// scheduled before this one has finished; it waits (griddepcontrol.wait, which returns once
+// the previous kernel has completed and its writes are visible) before it reads or writes
+// anything the previous kernel touches, and every CTA of it waits before it exits.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Candidate masks, prefix counts, bound and master check (run by the last prep CTA).
 __device__ void build_candidates(const EncArgs& a, const int32_t* master) {
@@ -99,6 +110,7 @@ __device__ void build_candidates(const EncArgs& a, const int32_t* master) {
 __global__ void __launch_bounds__(1024) enc_prep_kernel(EncArgs a, const int32_t* master) {
   extern __shared__ unsigned smask[];
   __shared__ int s_last;
+  pdl_trigger();   // the main kernel may start its canonical reads meanwhile
   const int i = blockIdx.x;
   const int S = a.rd.S, nb = a.rd.nb, k = a.k, nbw = a.sc.nbw;
   uint32_t* bits = a.sc.selbits + static_cast<int64_t>(i) * nb;
@@ -144,35 +156,51 @@ __device__ __forceinline__ int64_t cand_place(const EncArgs& a, int i, int li, i
          a.sc.word_prefix[i * nbw + (b >> 5)] + __popc(below);
 }
 
-// Exclusive prefix sum of the per-(agent, layer) record counts -> rowptr (one CTA).
+// Exclusive prefix sum of the per-(agent, layer) record counts -> rowptr (one CTA), in
+// chunks of kPrefixPer rows a thread whose counts are all loaded at once.
+constexpr int kPrefixPer = 8;
+
 __device__ void rows_prefix(const EncArgs& a) {
   __shared__ long long wsum[32];
   const int R = a.rd.N * a.nl;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int per = (R + blockDim.x - 1) / blockDim.x;
-  const int r0 = threadIdx.x * per, r1 = min(R, r0 + per);
-  long long local = 0;
-  for (int r = r0; r < r1; ++r) local += __ldcg(a.sc.row_count + r);
-  long long incl = local;
+  const int over = *a.over;
+  const int64_t bound = *a.bound;
+  long long carry = 0;
+  for (int c0 = 0; c0 < R; c0 += blockDim.x * kPrefixPer) {
+    const int r0 = c0 + threadIdx.x * kPrefixPer;
+    int cnt[kPrefixPer];
+    long long local = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += y;
+    for (int q = 0; q < kPrefixPer; ++q) {
+      cnt[q] = r0 + q < R ? __ldcg(a.sc.row_count + r0 + q) : 0;
+      local += cnt[q];
+    }
+    long long incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    long long before = 0, total = 0;
+    for (int w = 0; w < nw; ++w) {
+      if (w < wid) before += wsum[w];
+      total += wsum[w];
+    }
+    long long run = carry + before + incl - local;
+#pragma unroll
+    for (int q = 0; q < kPrefixPer; ++q) {
+      if (r0 + q < R) a.store.rowptr[r0 + q] = run;
+      run += cnt[q];
+    }
+    carry += total;
+    __syncthreads();   // wsum is rewritten by the next chunk
   }
-  if (lane == 31) wsum[wid] = incl;
-  __syncthreads();
-  long long before = 0;
-  for (int w = 0; w < wid; ++w) before += wsum[w];
-  long long run = before + incl - local;
-  for (int r = r0; r < r1; ++r) {
-    a.store.rowptr[r] = run;
-    run += __ldcg(a.sc.row_count + r);
-  }
-  if (threadIdx.x == blockDim.x - 1) {
-    long long total = 0;
-    for (int w = 0; w < nw; ++w) total += wsum[w];
-    a.store.rowptr[R] = total;
-    if (!*a.over && total != *a.bound) *a.sc.need_fixup = 1;
+  if (threadIdx.x == 0) {
+    a.store.rowptr[R] = carry;
+    if (!over && carry != bound) *a.sc.need_fixup = 1;
   }
 }
 
@@ -320,8 +348,9 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
   const int N = a.rd.N, nb = a.rd.nb, nbw = a.sc.nbw;
   const int lane = threadIdx.x & 31;
 
+  pdl_trigger();
   // the raw per-agent facts of this block for one chunk of agents, copied in by the first
-  // warp: the first chunk's copies leave at once and travel with the canonical rows
+  // warp once prep has finished
   __shared__ unsigned s_word[kAgentChunk], s_sb[kAgentChunk];
   __shared__ int s_fr[kAgentChunk], s_wp[kAgentChunk];
   __shared__ int64_t s_ap[kAgentChunk + 1];
@@ -337,10 +366,11 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
     if (lane == 0) cp_async8(&s_ap[n], a.sc.agent_prefix + c0 + n);
     cp_async_commit();
   };
-  if (threadIdx.x < 32) fetch_facts(0, min(kAgentChunk, N));
-
+  // the canonical rows are inputs: read before prep has finished
   HalfTile<kItems> h;
   load_half<kItems>(a, li, t0, tb0, kv, un.q0, h);
+  pdl_wait();
+  if (threadIdx.x < 32) fetch_facts(0, min(kAgentChunk, N));
   const int m = *a.m_ok;
   if (m < 0) {
     cp_async_wait<0>();
@@ -460,30 +490,47 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
   }
 }
 
-// One CTA after the main kernel: every (agent, layer) row's record count from the flags
-// (one warp per row), then their exclusive prefix sum -> rowptr and the fix-up decision.
-__global__ void __launch_bounds__(1024) enc_rows_kernel(EncArgs a) {
-  if (*a.m_ok < 0) return;
+// After the main kernel: every (agent, layer) row's record count from its flags, one warp
+// per row, spread over CTAs; the CTA that finishes last (a self-resetting counter; no CTA
+// waits) takes their exclusive prefix sum -> rowptr and decides on the fix-up.
+constexpr int kRowsThreads = 256;
+constexpr int kRowsPerWarp = 4;   // rows a warp counts at once: their loads are all in flight
+
+__global__ void __launch_bounds__(kRowsThreads) enc_rows_kernel(EncArgs a) {
+  __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
+  // the flags are zeroed by prep whatever the master, so counting starts at once; the
+  // master's check decides only whether the record rows are written
+  const int m_ok = *a.m_ok;
   const int R = a.rd.N * a.nl, nb = a.rd.nb;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  constexpr int kRows = 4;   // rows a warp counts at once: their loads are all in flight
-  for (int r0 = wid * kRows; r0 < R; r0 += nw * kRows) {
-    int cnt[kRows];
+  for (int r0 = (blockIdx.x * nw + wid) * kRowsPerWarp; r0 < R;
+       r0 += gridDim.x * nw * kRowsPerWarp) {
+    int cnt[kRowsPerWarp];
 #pragma unroll
-    for (int q = 0; q < kRows; ++q) cnt[q] = 0;
+    for (int q = 0; q < kRowsPerWarp; ++q) cnt[q] = 0;
     for (int b = lane; b < nb; b += 32)
 #pragma unroll
-      for (int q = 0; q < kRows; ++q)
+      for (int q = 0; q < kRowsPerWarp; ++q)
         if (r0 + q < R) cnt[q] += __ldcg(a.sc.flag + static_cast<int64_t>(r0 + q) * nb + b) != 0u;
 #pragma unroll
-    for (int q = 0; q < kRows; ++q) {
+    for (int q = 0; q < kRowsPerWarp; ++q) {
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) cnt[q] += __shfl_xor_sync(0xFFFFFFFFu, cnt[q], o);
       if (lane == 0 && r0 + q < R) a.sc.row_count[r0 + q] = cnt[q];
     }
   }
   __syncthreads();
-  rows_prefix(a);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.rows_done, 1) == static_cast<int>(gridDim.x) - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;                        // uniform across the CTA
+  __threadfence();
+  if (threadIdx.x == 0) *a.rows_done = 0;     // ready for the next call
+  if (m_ok >= 0) rows_prefix(a);
 }
 
 // Only when some candidate equalled the Master's block (need_fixup): (1) compact every
@@ -493,6 +540,7 @@ __global__ void __launch_bounds__(1024) enc_rows_kernel(EncArgs a) {
 // (1). Grid-stride; returns at once in the common case.
 template <int kItems>
 __global__ void __launch_bounds__(256) enc_fixup_kernel(EncArgs a, int tiles_per_layer) {
+  pdl_wait();
   if (__ldcg(a.sc.need_fixup) == 0) return;
   const int m = *a.m_ok;
   if (m < 0 || *a.over) return;
@@ -547,6 +595,24 @@ __global__ void __launch_bounds__(256) enc_fixup_kernel(EncArgs a, int tiles_per
   }
 }
 
+// Launches `kernel` so that it may be scheduled while the stream's previous kernel is still
+// running (programmatic stream serialization); the kernel waits for it where it must.
+template <typename... P, typename... A>
+static cudaError_t launch_after(void (*kernel)(P...), unsigned grid, int threads, size_t smem,
+                                cudaStream_t st, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int kItems>
 static cudaError_t run_tiles(const EncArgs& a, int threads, cudaStream_t st) {
   const int tpl = a.rd.nb * (a.rd.B / kTile);   // whole diff blocks: tails are zeroed
@@ -565,13 +631,15 @@ static cudaError_t run_tiles(const EncArgs& a, int threads, cudaStream_t st) {
     if (e0 != cudaSuccess) return e0;
     opted_in_device = cur;
   }
-  enc_main_kernel<kItems><<<static_cast<unsigned>(units), threads, stage, st>>>(a, tpl);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_after(enc_main_kernel<kItems>, static_cast<unsigned>(units), threads,
+                               stage, st, a, tpl);
   if (e != cudaSuccess) return e;
-  enc_rows_kernel<<<1, 1024, 0, st>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  enc_fixup_kernel<kItems><<<152, 256, 0, st>>>(a, tpl);
-  return cudaGetLastError();
+  const int rows = a.rd.N * a.nl;
+  const int per_cta = (kRowsThreads / 32) * kRowsPerWarp;
+  e = launch_after(enc_rows_kernel, static_cast<unsigned>((rows + per_cta - 1) / per_cta),
+                   kRowsThreads, 0, st, a);
+  if (e != cudaSuccess) return e;
+  return launch_after(enc_fixup_kernel<kItems>, 152u, 256, 0, st, a, tpl);
 }
 
 cudaError_t launch_encode(const Geom& g, const RoundDev& rd, const int32_t* master,
@@ -594,6 +662,7 @@ cudaError_t launch_encode(const Geom& g, const RoundDev& rd, const int32_t* mast
   a.m_ok = sc.need_fixup + 1;   // the context lays these ints out after need_fixup
   a.over = sc.need_fixup + 2;
   a.prep_done = sc.need_fixup + 3;
+  a.rows_done = sc.need_fixup + 4;
   a.bound = bound_dev;
   a.err = err;
   if (nl <= 0) return cudaSuccess;

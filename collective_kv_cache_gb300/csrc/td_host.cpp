@@ -47,7 +47,7 @@ struct td_ctx {
   int32_t* d_wprefix = nullptr;     // [max_agents * nbw_max + max_agents]
   int64_t* d_aprefix = nullptr;     // [max_agents + 1]
   uint32_t* d_flag = nullptr;       // [max_agents * L * max_nb] flags + [max_agents * L] counts
-  int32_t* d_ints = nullptr;        // need_fixup, m_ok, over, prep_done, (unused),
+  int32_t* d_ints = nullptr;        // need_fixup, m_ok, over, prep_done, rows_done,
                                     // pick_master's counter, spare
   int64_t* d_bound = nullptr;
   uint32_t* d_err = nullptr;
