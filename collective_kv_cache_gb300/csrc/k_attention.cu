@@ -128,6 +128,7 @@ template <int D, bool kFromPool>
 __global__ void __launch_bounds__(32, 13)
 attn_unit_kernel(const __grid_constant__ AttnArgs A, const __grid_constant__ AttnList list,
                  const __grid_constant__ AttnMaps maps) {
+  pdl_wait();
   constexpr int KCH = D / 16;         // k-chunks of one q.k product
   constexpr int HALVES = D / 64;      // 64-column boxes per row (a box row is 128 bytes)
   constexpr int BOX = kAttnStage * 128;               // one box: 16 rows x 128 bytes
@@ -427,6 +428,7 @@ attn_unit_kernel(const __grid_constant__ AttnArgs A, const __grid_constant__ Att
 // the output row and the natural-log sum of exponentials of the scaled scores.
 template <int D>
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs A, AttnList list) {
+  pdl_wait();
   constexpr int DPL = D / 32;
   const int lane = threadIdx.x & 31;
   const int64_t w = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
@@ -494,12 +496,12 @@ static cudaError_t run_attn(const AttnArgs& a, const AttnList& list, const AttnM
                             cudaStream_t st) {
   const int64_t units = static_cast<int64_t>(a.nl) * a.g.H * list.base[list.n];
   if (units == 0) return cudaSuccess;
-  attn_unit_kernel<D, kFromPool><<<static_cast<unsigned>(units), 32, 0, st>>>(a, list, maps);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_after(attn_unit_kernel<D, kFromPool>, static_cast<unsigned>(units), 32,
+                               0, st, a, list, maps);
   if (e != cudaSuccess) return e;
   const int64_t rows = static_cast<int64_t>(a.nl) * list.n * a.nq;
-  attn_combine_kernel<D><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, st>>>(a, list);
-  return cudaGetLastError();
+  return launch_after(attn_combine_kernel<D>, static_cast<unsigned>((rows + 3) / 4), 128, 0, st,
+                      a, list);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, const AttnList& list, const AttnMaps& maps,

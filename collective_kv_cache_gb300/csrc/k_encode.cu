@@ -51,15 +51,6 @@ struct EncArgs {
   uint32_t* err;
 };
 
-// Programmatic dependent launch within the encode: the next kernel of the stream may be
-// scheduled before this one has finished; it waits (griddepcontrol.wait, which returns once
-// the previous kernel has completed and its writes are visible) before it reads or writes
-// anything the previous kernel touches, and every CTA of it waits before it exits.
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Candidate masks, prefix counts, bound and master check (run by the last prep CTA).
 __device__ void build_candidates(const EncArgs& a, const int32_t* master) {
   const int N = a.rd.N, nbw = a.sc.nbw;
@@ -110,7 +101,10 @@ __device__ void build_candidates(const EncArgs& a, const int32_t* master) {
 __global__ void __launch_bounds__(1024) enc_prep_kernel(EncArgs a, const int32_t* master) {
   extern __shared__ unsigned smask[];
   __shared__ int s_last;
-  pdl_trigger();   // the main kernel may start its canonical reads meanwhile
+  // once every earlier kernel has finished (so the canonical rows are final), the main
+  // kernel may start reading them while prep runs
+  pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   const int S = a.rd.S, nb = a.rd.nb, k = a.k, nbw = a.sc.nbw;
   uint32_t* bits = a.sc.selbits + static_cast<int64_t>(i) * nb;
@@ -366,7 +360,7 @@ __global__ void __launch_bounds__(256, 3) enc_main_kernel(EncArgs a, int tiles_p
     if (lane == 0) cp_async8(&s_ap[n], a.sc.agent_prefix + c0 + n);
     cp_async_commit();
   };
-  // the canonical rows are inputs: read before prep has finished
+  // the canonical rows are inputs, final once prep has started: read before it finishes
   HalfTile<kItems> h;
   load_half<kItems>(a, li, t0, tb0, kv, un.q0, h);
   pdl_wait();
@@ -595,24 +589,6 @@ __global__ void __launch_bounds__(256) enc_fixup_kernel(EncArgs a, int tiles_per
   }
 }
 
-// Launches `kernel` so that it may be scheduled while the stream's previous kernel is still
-// running (programmatic stream serialization); the kernel waits for it where it must.
-template <typename... P, typename... A>
-static cudaError_t launch_after(void (*kernel)(P...), unsigned grid, int threads, size_t smem,
-                                cudaStream_t st, A... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(static_cast<unsigned>(threads));
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 template <int kItems>
 static cudaError_t run_tiles(const EncArgs& a, int threads, cudaStream_t st) {
   const int tpl = a.rd.nb * (a.rd.B / kTile);   // whole diff blocks: tails are zeroed
@@ -666,8 +642,8 @@ cudaError_t launch_encode(const Geom& g, const RoundDev& rd, const int32_t* mast
   a.bound = bound_dev;
   a.err = err;
   if (nl <= 0) return cudaSuccess;
-  enc_prep_kernel<<<rd.N, 1024, sc.nbw * sizeof(unsigned), st>>>(a, master);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_after(enc_prep_kernel, static_cast<unsigned>(rd.N), 1024,
+                               sc.nbw * sizeof(unsigned), st, a, master);
   if (e != cudaSuccess) return e;
   if (tile_items(g) == 1) return run_tiles<1>(a, tile_threads(g), st);
   return run_tiles<2>(a, tile_threads(g), st);

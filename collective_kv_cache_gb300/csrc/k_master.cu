@@ -15,6 +15,7 @@ __global__ void __launch_bounds__(1024)
 pick_master_kernel(const int32_t* __restrict__ sel, int N, int S, int B, int k, int nbw,
                    int64_t* __restrict__ cost_out, int32_t* __restrict__ master,
                    uint32_t* gmask, int* done, uint32_t* err) {
+  pdl_wait();
   extern __shared__ unsigned char smem_raw[];
   unsigned* mask = reinterpret_cast<unsigned*>(smem_raw);            // [N][nbw] (last CTA)
   __shared__ int s_last;
@@ -88,9 +89,8 @@ cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int B, int k, i
     if (e != cudaSuccess) return e;
   }
   const int threads = k >= 512 ? 1024 : 256;
-  pick_master_kernel<<<N, threads, smem, st>>>(sel, N, S, B, k, nbw, cost, master, gmask, done,
-                                               err);
-  return cudaGetLastError();
+  return launch_after(pick_master_kernel, static_cast<unsigned>(N), threads, smem, st, sel, N, S,
+                      B, k, nbw, cost, master, gmask, done, err);
 }
 
 }  // namespace td

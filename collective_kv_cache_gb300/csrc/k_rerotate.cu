@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(256, 4)
 rerotate_kernel(Geom g, RoundDev rd, PoolDev pool, const uint16_t* __restrict__ kc,
                 const uint16_t* __restrict__ vc, int layer_begin, int tiles_per_layer,
                 uint32_t* err) {
+  pdl_wait();
   __shared__ int64_t s_row[kAgentChunk * kTile];  // pool row of (agent, token)
   const Unit un = unit_of(g, blockIdx.x, tiles_per_layer);
   if (un.kv == 1 && vc == nullptr) return;
@@ -91,12 +92,10 @@ cudaError_t launch_rerotate(const Geom& g, const RoundDev& rd, const PoolDev& po
   const int64_t units = static_cast<int64_t>(tpl) * nl * 2 * parts_per_tile(g);
   if (units == 0) return cudaSuccess;
   if (tile_items(g) == 1)
-    rerotate_kernel<1><<<static_cast<unsigned>(units), tile_threads(g), 0, st>>>(
-        g, rd, pool, kc, vc, layer_begin, tpl, err);
-  else
-    rerotate_kernel<2><<<static_cast<unsigned>(units), tile_threads(g), 0, st>>>(
-        g, rd, pool, kc, vc, layer_begin, tpl, err);
-  return cudaGetLastError();
+    return launch_after(rerotate_kernel<1>, static_cast<unsigned>(units), tile_threads(g), 0, st,
+                        g, rd, pool, kc, vc, layer_begin, tpl, err);
+  return launch_after(rerotate_kernel<2>, static_cast<unsigned>(units), tile_threads(g), 0, st,
+                      g, rd, pool, kc, vc, layer_begin, tpl, err);
 }
 
 }  // namespace td

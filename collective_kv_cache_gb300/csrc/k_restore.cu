@@ -17,6 +17,7 @@ template <int kItems, bool kRotate>
 __global__ void __launch_bounds__(256, 3)
 restore_kernel(Geom g, RoundDev rd, PoolDev pool, StoreDev store, AgentList agents,
                int layer_begin, int store_layer0, int tiles_per_layer, uint32_t* err) {
+  pdl_wait();
   __shared__ int64_t s_row[kAgentChunk * kTile];  // pool row of (agent, token)
   __shared__ int s_rec[kAgentChunk];               // record of (agent), -1 none, -2 bad
   const Unit un = unit_of(g, blockIdx.x, tiles_per_layer);
@@ -119,12 +120,12 @@ static cudaError_t go(const Geom& g, const RoundDev& rd, const PoolDev& pool,
   const int64_t units = static_cast<int64_t>(tpl) * nl * 2 * parts_per_tile(g);
   if (units == 0 || agents.n == 0) return cudaSuccess;
   if (frame == 0)
-    restore_kernel<kItems, true><<<static_cast<unsigned>(units), tile_threads(g), 0, st>>>(
-        g, rd, pool, store, agents, layer_begin, store_layer0, tpl, err);
-  else
-    restore_kernel<kItems, false><<<static_cast<unsigned>(units), tile_threads(g), 0, st>>>(
-        g, rd, pool, store, agents, layer_begin, store_layer0, tpl, err);
-  return cudaGetLastError();
+    return launch_after(restore_kernel<kItems, true>, static_cast<unsigned>(units),
+                        tile_threads(g), 0, st, g, rd, pool, store, agents, layer_begin,
+                        store_layer0, tpl, err);
+  return launch_after(restore_kernel<kItems, false>, static_cast<unsigned>(units),
+                      tile_threads(g), 0, st, g, rd, pool, store, agents, layer_begin,
+                      store_layer0, tpl, err);
 }
 
 cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& pool,
@@ -143,6 +144,7 @@ cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& poo
 __global__ void __launch_bounds__(256)
 materialise_kernel(int E, int S, int B, int nb, StoreDev store, int agent, int sl0,
                    uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, uint32_t* err) {
+  pdl_wait();
   const int kv = blockIdx.x & 1;
   const int b = (blockIdx.x >> 1) % nb;
   const int li = (blockIdx.x >> 1) / nb;
@@ -168,9 +170,8 @@ cudaError_t launch_materialise(const Geom& g, const RoundDev& rd, const StoreDev
                                uint32_t* err, cudaStream_t st) {
   const int64_t units = static_cast<int64_t>(nl) * rd.nb * 2;
   if (units == 0) return cudaSuccess;
-  materialise_kernel<<<static_cast<unsigned>(units), 256, 0, st>>>(g.E, rd.S, rd.B, rd.nb, store,
-                                                                   agent, sl0, dk, dv, err);
-  return cudaGetLastError();
+  return launch_after(materialise_kernel, static_cast<unsigned>(units), 256, 0, st, g.E, rd.S,
+                      rd.B, rd.nb, store, agent, sl0, dk, dv, err);
 }
 
 }  // namespace td

@@ -63,6 +63,7 @@ __device__ __forceinline__ void deviation_token(const Geom& g, const RoundDev& r
 __global__ void __launch_bounds__(256)
 deviation_kernel(Geom g, RoundDev rd, PoolDev pool, int check_layer,
                  const uint16_t* __restrict__ kf, float* __restrict__ dev, uint32_t* err) {
+  pdl_wait();
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (w >= static_cast<int64_t>(rd.N) * rd.S) return;
   deviation_token(g, rd, pool, check_layer, kf, dev, w, threadIdx.x & 31, err);
@@ -161,6 +162,7 @@ __device__ void select_agent(const float* dev_i, int S, int k, int32_t* out, uns
 
 __global__ void __launch_bounds__(1024)
 select_kernel(const float* __restrict__ dev, int S, int k, int32_t* __restrict__ sel) {
+  pdl_wait();
   __shared__ __align__(16) unsigned hist[256];
   __shared__ int warp_tot[32];
   __shared__ int s_total, s_remaining;
@@ -176,16 +178,14 @@ cudaError_t launch_deviation(const Geom& g, const RoundDev& rd, const PoolDev& p
   const int64_t warps = static_cast<int64_t>(rd.N) * rd.S;
   if (warps == 0) return cudaSuccess;
   const int64_t blocks = (warps * 32 + 255) / 256;
-  deviation_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(g, rd, pool, check_layer,
-                                                                  k_fresh, dev, err);
-  return cudaGetLastError();
+  return launch_after(deviation_kernel, static_cast<unsigned>(blocks), 256, 0, st, g, rd, pool,
+                      check_layer, k_fresh, dev, err);
 }
 
 cudaError_t launch_select(const float* dev, int N, int S, int k, int32_t* sel,
                           cudaStream_t st) {
   if (k <= 0 || N <= 0) return cudaSuccess;
-  select_kernel<<<N, 1024, 0, st>>>(dev, S, k, sel);
-  return cudaGetLastError();
+  return launch_after(select_kernel, static_cast<unsigned>(N), 1024, 0, st, dev, S, k, sel);
 }
 
 cudaError_t launch_check_select(const Geom& g, const RoundDev& rd, const PoolDev& pool,

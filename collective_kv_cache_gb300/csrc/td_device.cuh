@@ -128,6 +128,34 @@ __device__ __forceinline__ Unit unit_of(const Geom& g, int64_t idx, int tiles_pe
 }
 
 // Agents handled per shared-memory chunk by the tile kernels (row table 64 x 16 x 8 B).
+// Programmatic dependent launch: a kernel launched by launch_after may be scheduled while
+// the stream's previous kernel is finishing. pdl_wait() returns once that kernel has
+// completed and its writes are visible; a kernel calls it before it touches memory that
+// earlier work may write (every kernel here that is launched this way does so first thing,
+// except where its comment says what it reads before), and every CTA calls it before it
+// exits, so that a kernel's completion still implies its predecessors'. pdl_trigger() lets
+// the next kernel be scheduled before this one's CTAs have exited.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... P, typename... A>
+inline cudaError_t launch_after(void (*kernel)(P...), unsigned grid, int threads, size_t smem,
+                                cudaStream_t st, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kAgentChunk = 64;
 
 // Row index (in elements / E) of the token at prompt position `pos` of `agent`, layer and
