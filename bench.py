@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 METRIC = "restore+reuse KV GB/s (% of GB300 HBM peak); agent-rounds/sec, 7B shape"
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal (the measured copy peak is the roofline)
-LAUNCHES_PER_STEP = 9    # rerotate 1, deviation + top-k 2, master 1, encode 4, restore 1
+LAUNCHES_PER_STEP = 8    # rerotate 1, deviation + top-k 1, master 1, encode 4, restore 1
 # DRAM bytes (read + write) per launch of the roofline kernels at the benchmarked size, from
 # one ncu capture of these kernels as they are now (dram__bytes_read.sum +
 # dram__bytes_write.sum); set an entry to None when its kernel changes.
@@ -785,7 +785,7 @@ def report_chunked(args, cfg, seed, device, rank, world):
                          "frac": round(by[dom] / (stage_ms[dom] * 1e-3) / 1e9 / peak, 4),
                          "traffic": None, "peak_kind": peak_kind},
             "storage": storage_ratios(cfg, nnz, L),
-            "gpu_launches": args.steps * (4 + 5 * ((L + args.chunk_layers - 1) // args.chunk_layers)),
+            "gpu_launches": args.steps * (3 + 5 * ((L + args.chunk_layers - 1) // args.chunk_layers)),
             "clocks": clk.summary(),
             "e2e": None, "cpu_baseline": None,
         }

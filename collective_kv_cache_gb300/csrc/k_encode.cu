@@ -270,19 +270,6 @@ __device__ __forceinline__ void store_item(const EncArgs& a, int kv, int64_t rec
   st16(dst + h.e0[r] + a.g.half, x1);
 }
 
-// ---- per-thread asynchronous staging of recomputed rows (cp.async, 16 bytes a copy)
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int kPending>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
-}
-
 constexpr int kStageDepth = 3;   // candidates in flight per thread
 
 // Stage, for candidate agent `ag`, the recomputed data of this thread's selected items:

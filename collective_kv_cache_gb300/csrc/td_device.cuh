@@ -156,6 +156,33 @@ inline cudaError_t launch_after(void (*kernel)(P...), unsigned grid, int threads
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// ---- per-thread asynchronous copies into shared memory (cp.async, 16 bytes a copy). A
+// thread that reads back only the cells it copied itself needs no barrier, only the wait.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+// The same copy with an L2 cache policy (from l2_evict_first()).
+__device__ __forceinline__ void cp_async16_hint(void* smem, const void* gmem, uint64_t policy) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem),
+               "l"(policy)
+               : "memory");
+}
+// An L2 policy under which the lines a load brings in are the first to be evicted.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
 constexpr int kAgentChunk = 64;
 
 // Row index (in elements / E) of the token at prompt position `pos` of `agent`, layer and

@@ -37,6 +37,8 @@ struct td_ctx {
 
   // scratch
   float* d_dev = nullptr;           // [max_agents * max_shared]
+  uint32_t* d_sel_hist = nullptr;   // [max_agents * kSelHistBins] selection histograms (zero)
+  int32_t* d_sel_done = nullptr;    // [max_agents] selection counters (zero)
   float* d_gdev = nullptr;          // [max_shared] group deviation (variant)
   double* d_score = nullptr;        // [max_agents] deviation totals (variant)
   uint32_t* d_selbits = nullptr;    // [max_agents * max_nb]
@@ -77,6 +79,8 @@ void free_ctx(td_ctx* c) {
   cudaFree(c->d_tok_block);
   cudaFree(c->d_blk_start);
   cudaFree(c->d_dev);
+  cudaFree(c->d_sel_hist);
+  cudaFree(c->d_sel_done);
   cudaFree(c->d_gdev);
   cudaFree(c->d_score);
   cudaFree(c->d_selbits);
@@ -460,6 +464,8 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   chk(cudaMalloc(&c->d_tok_block, static_cast<size_t>(max_shared) * 4));
   chk(cudaMalloc(&c->d_blk_start, static_cast<size_t>(max_blocks) * 4));
   chk(cudaMalloc(&c->d_dev, NS * 4));
+  chk(cudaMalloc(&c->d_sel_hist, static_cast<size_t>(max_agents) * kSelHistBins * 4));
+  chk(cudaMalloc(&c->d_sel_done, static_cast<size_t>(max_agents) * 4));
   chk(cudaMalloc(&c->d_gdev, static_cast<size_t>(max_shared) * 4));
   chk(cudaMalloc(&c->d_score, static_cast<size_t>(max_agents) * 8));
   chk(cudaMalloc(&c->d_selbits, static_cast<size_t>(max_agents) * max_nb * 4));
@@ -479,6 +485,9 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   chk(cudaEventCreateWithFlags(&c->stage_done, cudaEventDisableTiming));
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->d_ints, 0, 8 * sizeof(int32_t));
+  if (e == cudaSuccess)
+    e = cudaMemset(c->d_sel_hist, 0, static_cast<size_t>(max_agents) * kSelHistBins * 4);
+  if (e == cudaSuccess) e = cudaMemset(c->d_sel_done, 0, static_cast<size_t>(max_agents) * 4);
   if (e != cudaSuccess) {
     free_ctx(c);
     return TD_ERR_CUDA;
@@ -554,7 +563,7 @@ td_status td_check_select(td_ctx* c, const td_round* r, int32_t check_layer,
   const RoundDev rd = round_dev(c);
   return cuda_status(launch_check_select(c->g, rd, pd, check_layer,
                                          static_cast<const uint16_t*>(k_fresh), dev, k, sel,
-                                         c->d_err, st));
+                                         c->d_sel_hist, c->d_sel_done, c->d_err, st));
 }
 
 td_status td_pick_master(td_ctx* c, const td_round* r, const int32_t* sel, int32_t k,

@@ -60,6 +60,9 @@ CASES = {
     "qwen7b_b32_p32_3layers": synth.qwen7b().replace(n_layers=3, diff_block=32, page_size=32),
     "density40_b32_p32_8agents_2layers": synth.density(40, page_size=32, pool_bytes=None).replace(
         n_agents=8, n_layers=2, diff_block=32),
+    # a shared span beyond one cluster's reach (the selection's many-CTA form), ragged
+    "mini_long_span": _mini(n_agents=3, n_layers=2, block_lens=(9000, 6999, 4002), seed=89,
+                            hist_range=(0, 300)),
 }
 
 
