@@ -876,24 +876,23 @@ def oracle_step(sub, rnd, kc, vc, orc, cache):
     The synthetic recompute (reused K plus noise) is built on the first pass and reused;
     it is not timed."""
     import oracle
-    from tests import roundkit as rk  # test-side assembly of the synthetic recompute
+    from collective_kv_cache_gb300 import synth
     desc = (rnd.block_len, rnd.hist_len, rnd.perm)
-    if "chain" not in cache:
-        off = orc.offsets(*desc)
-        cache["chain"] = rk.Chain(sub, rnd, desc, off, rk.positions(off, rnd.block_len), kc, vc)
-    ch = cache["chain"]
+    if "pos" not in cache:
+        cache["pos"] = synth.positions(orc.offsets(*desc), rnd.block_len)
+    pos = cache["pos"]
     pool = oracle.new_pool(sub, rnd.num_pages)
     t0 = time.perf_counter()
     assert orc.rerotate(sub, desc, kc, vc, pool, rnd.num_pages, rnd.block_table) == 0
     secs = time.perf_counter() - t0
     if "kf" not in cache:
-        cache["kf"] = rk.fresh_check(ch, pool)
+        cache["kf"] = synth.recompute_check(sub, rnd, pos, pool)
     t0 = time.perf_counter()
     st, sel, _ = orc.check_select(sub, desc, pool, rnd.num_pages, rnd.block_table, cache["kf"])
     m, _ = orc.pick_master(sub.n_shared, sub.diff_block, sel)
     secs += time.perf_counter() - t0
     if "kfs" not in cache:
-        cache["kfs"], cache["vfs"] = rk.fresh_selected(ch, pool, sel)
+        cache["kfs"], cache["vfs"] = synth.recompute_selected(sub, rnd, pos, pool, vc, sel)
     pool2 = oracle.new_pool(sub, rnd.num_pages)
     t0 = time.perf_counter()
     store = orc.diff_encode(sub, desc, m, kc, vc, sel, cache["kfs"], cache["vfs"])

@@ -30,6 +30,19 @@ struct td_ctx {
   cudaEvent_t stage_done = nullptr;
   bool stage_pending = false;
 
+  // Streams that have read the round tables since their last upload, each with an event
+  // recorded after its latest launch. A round change makes the uploading stream wait on
+  // all of them; a stream's first call after an upload waits on tables_ready.
+  struct StreamUse {
+    cudaStream_t stream;
+    cudaEvent_t last_use;
+    bool ordered;      // ordered after the current tables' upload
+  };
+  std::vector<StreamUse> users;
+  cudaEvent_t tables_ready = nullptr;
+  cudaStream_t tables_stream = nullptr;
+  bool tables_recorded = false;
+
   // cached round (host copy) and its device view
   bool have_round = false;
   int N = 0, M = 0, S = 0;
@@ -69,8 +82,6 @@ int log2i(int x) {
   return s;
 }
 
-td_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TD_OK : TD_ERR_CUDA; }
-
 void free_ctx(td_ctx* c) {
   if (!c) return;
   cudaFree(c->d_off);
@@ -98,6 +109,8 @@ void free_ctx(td_ctx* c) {
   if (c->h_stage) cudaFreeHost(c->h_stage);
   if (c->h_words) cudaFreeHost(c->h_words);
   if (c->stage_done) cudaEventDestroy(c->stage_done);
+  if (c->tables_ready) cudaEventDestroy(c->tables_ready);
+  for (auto& u : c->users) cudaEventDestroy(u.last_use);
   delete c;
 }
 
@@ -106,7 +119,66 @@ bool same_device(const td_ctx* c) {
   return cudaGetDevice(&d) == cudaSuccess && d == c->device;
 }
 
-// Validates the round and brings the device tables up to date with it.
+bool capturing(cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+td_ctx::StreamUse* find_use(td_ctx* c, cudaStream_t st) {
+  for (auto& u : c->users)
+    if (u.stream == st) return &u;
+  return nullptr;
+}
+
+constexpr size_t kMaxTrackedStreams = 64;
+
+// The entry of `st` in the users list, created when missing (when the list is full, every
+// tracked stream is first drained on the host and the list starts over).
+td_ctx::StreamUse* use_of(td_ctx* c, cudaStream_t st) {
+  if (td_ctx::StreamUse* u = find_use(c, st)) return u;
+  if (c->users.size() >= kMaxTrackedStreams) {
+    for (auto& u : c->users) {
+      if (cudaEventSynchronize(u.last_use) != cudaSuccess) return nullptr;
+      cudaEventDestroy(u.last_use);
+    }
+    c->users.clear();
+  }
+  td_ctx::StreamUse u{st, nullptr, false};
+  if (cudaEventCreateWithFlags(&u.last_use, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  // a fresh event counts as complete: waiting on it before its first record is a no-op
+  c->users.push_back(u);
+  return &c->users.back();
+}
+
+// Orders `st` after the upload of the current tables (once per stream and upload).
+td_status order_after_tables(td_ctx* c, cudaStream_t st) {
+  td_ctx::StreamUse* u = use_of(c, st);
+  if (!u) return TD_ERR_CUDA;
+  if (u->ordered) return TD_OK;
+  if (c->tables_recorded && st != c->tables_stream &&
+      cudaStreamWaitEvent(st, c->tables_ready, 0) != cudaSuccess)
+    return TD_ERR_CUDA;
+  u->ordered = true;
+  return TD_OK;
+}
+
+// After a call's launches: its stream's reads of the tables end with this point.
+td_status note_use(td_ctx* c, cudaStream_t st) {
+  if (capturing(st)) return TD_OK;
+  td_ctx::StreamUse* u = find_use(c, st);
+  if (!u) return TD_OK;
+  return cudaEventRecord(u->last_use, st) == cudaSuccess ? TD_OK : TD_ERR_CUDA;
+}
+
+// Validates the round and brings the device tables up to date with it. The tables are
+// shared by every stream that uses the context: a stream is ordered after their upload
+// before its first launch, and a new upload waits (on the device) for every launch that
+// may still read the old tables. Inside a stream capture nothing is tracked and a change
+// of round is refused: the tables must already hold the round, uploaded and finished.
 td_status prepare_round(td_ctx* c, const td_round* r, cudaStream_t st) {
   if (!r || !r->block_len || !r->hist_len || !r->perm) return TD_ERR_INVALID_ARG;
   const int N = r->n_agents, M = r->n_blocks;
@@ -127,11 +199,18 @@ td_status prepare_round(td_ctx* c, const td_round* r, cudaStream_t st) {
       seen[j] = 1;
     }
   }
+  const bool cap = capturing(st);
   if (c->have_round && c->N == N && c->M == M &&
       std::memcmp(c->c_len.data(), r->block_len, sizeof(int32_t) * M) == 0 &&
       std::memcmp(c->c_hist.data(), r->hist_len, sizeof(int32_t) * N) == 0 &&
       std::memcmp(c->c_perm.data(), r->perm, sizeof(int32_t) * N * M) == 0)
-    return TD_OK;
+    return cap ? TD_OK : order_after_tables(c, st);
+  if (cap) return TD_ERR_INVALID_ARG;
+
+  // every launch that may still read the old tables finishes before they change
+  for (auto& u : c->users)
+    if (u.stream != st && cudaStreamWaitEvent(st, u.last_use, 0) != cudaSuccess)
+      return TD_ERR_CUDA;
 
   // the previous upload must have left the staging buffer before it is rewritten
   if (c->stage_pending) {
@@ -180,8 +259,13 @@ td_status prepare_round(td_ctx* c, const td_round* r, cudaStream_t st) {
       (e = cudaMemcpyAsync(c->d_sin, sn, n_off * half * 4, cudaMemcpyHostToDevice, st)) ||
       (e = cudaMemcpyAsync(c->d_tok_block, tokb, S * 4, cudaMemcpyHostToDevice, st)) ||
       (e = cudaMemcpyAsync(c->d_blk_start, bst, M * 4, cudaMemcpyHostToDevice, st)) ||
-      (e = cudaEventRecord(c->stage_done, st)))
+      (e = cudaEventRecord(c->stage_done, st)) ||
+      (e = cudaEventRecord(c->tables_ready, st)))
     return TD_ERR_CUDA;
+  c->tables_stream = st;
+  c->tables_recorded = true;
+  for (auto& u : c->users) u.ordered = false;
+  if (order_after_tables(c, st) != TD_OK) return TD_ERR_CUDA;
   c->stage_pending = true;
   c->have_round = true;
   c->N = N;
@@ -394,7 +478,7 @@ td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store
     a.part_ml = c->d_attn + static_cast<size_t>(units) * kAttnGMax * D;
     if (launch_attention(a, L, maps, store == nullptr, st) != cudaSuccess) return TD_ERR_CUDA;
   }
-  return TD_OK;
+  return note_use(c, st);
 }
 
 }  // namespace
@@ -483,6 +567,7 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   chk(cudaMallocHost(&c->h_stage, c->stage_bytes));
   chk(cudaMallocHost(&c->h_words, 4 * sizeof(int64_t)));
   chk(cudaEventCreateWithFlags(&c->stage_done, cudaEventDisableTiming));
+  chk(cudaEventCreateWithFlags(&c->tables_ready, cudaEventDisableTiming));
   if (e == cudaSuccess) e = cudaMemset(c->d_err, 0, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->d_ints, 0, 8 * sizeof(int32_t));
   if (e == cudaSuccess)
@@ -537,10 +622,11 @@ td_status td_rerotate_batched(td_ctx* c, const td_round* r, const void* k_canon,
   if (s != TD_OK) return s;
   PoolDev pd;
   if ((s = pool_dev(c, r, pool, &pd)) != TD_OK) return s;
-  return cuda_status(launch_rerotate(c->g, round_dev(c), pd,
-                                     static_cast<const uint16_t*>(k_canon),
-                                     static_cast<const uint16_t*>(v_canon), layer_begin,
-                                     layer_end - layer_begin, c->d_err, st));
+  if (launch_rerotate(c->g, round_dev(c), pd, static_cast<const uint16_t*>(k_canon),
+                      static_cast<const uint16_t*>(v_canon), layer_begin, layer_end - layer_begin,
+                      c->d_err, st) != cudaSuccess)
+    return TD_ERR_CUDA;
+  return note_use(c, st);
 }
 
 td_status td_check_select(td_ctx* c, const td_round* r, int32_t check_layer,
@@ -561,9 +647,10 @@ td_status td_check_select(td_ctx* c, const td_round* r, int32_t check_layer,
   *k_out = k;
   float* dev = dev_out ? dev_out : c->d_dev;
   const RoundDev rd = round_dev(c);
-  return cuda_status(launch_check_select(c->g, rd, pd, check_layer,
-                                         static_cast<const uint16_t*>(k_fresh), dev, k, sel,
-                                         c->d_sel_hist, c->d_sel_done, c->d_err, st));
+  if (launch_check_select(c->g, rd, pd, check_layer, static_cast<const uint16_t*>(k_fresh), dev,
+                          k, sel, c->d_sel_hist, c->d_sel_done, c->d_err, st) != cudaSuccess)
+    return TD_ERR_CUDA;
+  return note_use(c, st);
 }
 
 td_status td_pick_master(td_ctx* c, const td_round* r, const int32_t* sel, int32_t k,
@@ -577,7 +664,7 @@ td_status td_pick_master(td_ctx* c, const td_round* r, const int32_t* sel, int32
   if (k > c->S) return TD_ERR_INVALID_ARG;
   cudaError_t e = launch_pick_master(sel, c->N, c->S, c->shape.diff_block, k, cost_out, master_dev, c->d_pm_mask,
                                      c->d_ints + 5, c->d_err, st);
-  if (e != cudaSuccess) return TD_ERR_CUDA;
+  if (e != cudaSuccess || note_use(c, st) != TD_OK) return TD_ERR_CUDA;
   if (master_host) {
     int32_t* h = reinterpret_cast<int32_t*>(c->h_words);
     if ((e = cudaMemcpyAsync(h, master_dev, 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
@@ -605,10 +692,13 @@ td_status td_check_select_group(td_ctx* c, const td_round* r, int32_t check_laye
   const int k = static_cast<int>((static_cast<int64_t>(recompute_pct) * c->S + 99) / 100);
   if (k > 0 && !sel) return TD_ERR_INVALID_ARG;
   *k_out = k;
-  return cuda_status(launch_check_select_group(
-      c->g, round_dev(c), pd, check_layer, static_cast<const uint16_t*>(k_fresh),
-      dev_out ? dev_out : c->d_dev, group_dev_out ? group_dev_out : c->d_gdev, k, sel,
-      c->d_err, st));
+  if (launch_check_select_group(c->g, round_dev(c), pd, check_layer,
+                                static_cast<const uint16_t*>(k_fresh),
+                                dev_out ? dev_out : c->d_dev,
+                                group_dev_out ? group_dev_out : c->d_gdev, k, sel, c->d_err,
+                                st) != cudaSuccess)
+    return TD_ERR_CUDA;
+  return note_use(c, st);
 }
 
 td_status td_pick_master_min_deviation(td_ctx* c, const td_round* r, const int32_t* sel,
@@ -624,7 +714,7 @@ td_status td_pick_master_min_deviation(td_ctx* c, const td_round* r, const int32
   cudaError_t e = launch_min_dev_master(sel, dev, c->N, c->S, k,
                                         score_out ? score_out : c->d_score, master_dev,
                                         c->d_err, st);
-  if (e != cudaSuccess) return TD_ERR_CUDA;
+  if (e != cudaSuccess || note_use(c, st) != TD_OK) return TD_ERR_CUDA;
   if (master_host) {
     int32_t* h = reinterpret_cast<int32_t*>(c->h_words);
     if (cudaMemcpyAsync(h, master_dev, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -688,7 +778,7 @@ td_status td_diff_encode(td_ctx* c, const td_round* r, const int32_t* master,
                                 static_cast<const uint16_t*>(k_fresh_sel),
                                 static_cast<const uint16_t*>(v_fresh_sel), nl, sd, sc, c->d_err,
                                 c->d_bound, st);
-  if (e != cudaSuccess) return TD_ERR_CUDA;
+  if (e != cudaSuccess || note_use(c, st) != TD_OK) return TD_ERR_CUDA;
   store->layer_begin = layer_begin;
   store->layer_end = layer_end;
   if (nnz_out) {
@@ -747,7 +837,7 @@ td_status td_fused_restore(td_ctx* c, const td_round* r, const td_diff_store* st
                                    layer_end - layer_begin, frame, c->d_err, st);
     if (e != cudaSuccess) return TD_ERR_CUDA;
   }
-  return TD_OK;
+  return note_use(c, st);
 }
 
 td_status td_materialise_mirror(td_ctx* c, const td_round* r, const td_diff_store* store,
@@ -781,7 +871,7 @@ td_status td_materialise_mirror(td_ctx* c, const td_round* r, const td_diff_stor
                          layer_end - layer_begin, static_cast<uint16_t*>(dense_k),
                          static_cast<uint16_t*>(dense_v), c->d_err, st) != cudaSuccess)
     return TD_ERR_CUDA;
-  return TD_OK;
+  return note_use(c, st);
 }
 
 td_status td_fused_attention(td_ctx* c, const td_round* r, const td_diff_store* store,

@@ -39,10 +39,35 @@ constexpr size_t kScratchBytes = align256(kOffDev + 4 * size_t(kNaMaxDev));
 static __device__ __align__(256) unsigned char g_select_scratch[kScratchBytes];
 
 // Host code cannot use g_select_scratch as an address: it is a host-side stand-in. The
-// device address is looked up once per device and kept here.
+// device address is looked up with the device current and kept, per device, together with
+// the CUDA context it belongs to: after a device reset the device has a new context (and
+// the array a new address), so the address is looked up again.
 constexpr int kMaxDevices = 64;
 std::mutex g_addr_mu;
 unsigned char* g_addr[kMaxDevices] = {};
+void* g_addr_ctx[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+void* current_context() {
+  CUcontext c = nullptr;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get || get(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 cudaError_t scratch_address(unsigned char** out) {
   int dev = -1;
@@ -50,11 +75,14 @@ cudaError_t scratch_address(unsigned char** out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_addr_mu);
-  if (!g_addr[dev]) {
+  void* ctx = current_context();
+  if (!g_addr[dev] || !ctx || g_addr_ctx[dev] != ctx) {
+    // the lookup also creates the device's context if none is current yet
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_select_scratch);
     if (e != cudaSuccess) return e;
     g_addr[dev] = static_cast<unsigned char*>(p);
+    g_addr_ctx[dev] = current_context();
   }
   *out = g_addr[dev];
   return cudaSuccess;
@@ -104,8 +132,8 @@ extern "C" td_status td_check_select_noalloc(const td_shape* shape, const td_rou
     return TD_ERR_INVALID_ARG;
   const td_shape& s = *shape;
   if (s.n_layers < 1 || s.n_kv_heads < 1 || s.head_dim < 16 || s.head_dim % 16 != 0 ||
-      s.page_size < 1 || s.diff_block != kDiffBlock)
-    return TD_ERR_INVALID_ARG;
+      s.page_size < 1 || (s.diff_block != kDiffBlock && s.diff_block != kMaxDiffBlock))
+    return TD_ERR_INVALID_ARG;   // the selection does not depend on the diff block
   const int64_t E = static_cast<int64_t>(s.n_kv_heads) * s.head_dim;
   if (E > 2048) return TD_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k_fresh) & 15u) || (reinterpret_cast<uintptr_t>(pool->base) & 15u))
@@ -141,8 +169,9 @@ extern "C" td_status td_check_select_noalloc(const td_shape* shape, const td_rou
   if (scratch_address(&base) != cudaSuccess) return TD_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* err = reinterpret_cast<uint32_t*>(base + kOffErr);
-  // The round descriptor is copied from the caller's host arrays; a pageable-source copy
-  // has left the source when it returns.
+  // The round descriptor is copied from the caller's host arrays on the stream: from
+  // pageable memory the copy has read them when it returns, from page-locked memory it
+  // may read them later (the caller keeps them unchanged until the stream passes here).
   if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess ||
       cudaMemcpyAsync(base + kOffLen, r->block_len, 4 * size_t(M), cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(base + kOffHist, r->hist_len, 4 * size_t(N), cudaMemcpyHostToDevice, st) != cudaSuccess ||
@@ -161,8 +190,8 @@ extern "C" td_status td_check_select_noalloc(const td_shape* shape, const td_rou
   rd.N = N;
   rd.M = M;
   rd.S = static_cast<int>(S);
-  rd.B = kDiffBlock;
-  rd.nb = static_cast<int>((S + kDiffBlock - 1) / kDiffBlock);
+  rd.B = s.diff_block;
+  rd.nb = static_cast<int>((S + s.diff_block - 1) / s.diff_block);
   rd.nt = static_cast<int>((S + kTile - 1) / kTile);
   rd.off = reinterpret_cast<const int32_t*>(base + kOffOff);
   rd.cos_t = nullptr;  // the deviation pass turns nothing

@@ -32,7 +32,7 @@ class RoundRunner:
     def __init__(self, cfg, block_len, hist_len, perm, block_table: np.ndarray, num_pages: int,
                  device="cuda", stream: Optional[torch.cuda.Stream] = None,
                  pool_fill: Optional[int] = None, max_agents=None, max_blocks=None,
-                 max_shared=None):
+                 max_shared=None, ctx: Optional["td.Context"] = None):
         self.cfg = cfg
         self.device = torch.device(device)
         self.stream = stream or torch.cuda.current_stream(self.device)
@@ -40,8 +40,9 @@ class RoundRunner:
         self.S = int(np.sum(block_len))
         self.L, self.E, self.B = cfg.n_layers, cfg.elems, cfg.diff_block
         self.nb = (self.S + self.B - 1) // self.B
-        self.ctx = td.Context(td.make_shape(cfg), max_agents or self.N, max_blocks or self.M,
-                              max_shared or self.S)
+        # a context may be shared by several runners (rounds); it must fit each of them
+        self.ctx = ctx or td.Context(td.make_shape(cfg), max_agents or self.N,
+                                     max_blocks or self.M, max_shared or self.S)
         self.round = td.make_round(block_len, hist_len, perm)
         self._views = None
         self.num_pages = int(num_pages)
@@ -102,8 +103,8 @@ class RoundRunner:
         """One round with the check layer's selection overlapped: the check layer is
         re-rotated first; selection and master choice run on `side` while the other layers
         are re-rotated on the main stream; encode and restore follow on the main stream.
-        Calls on one context may overlap like this because they touch disjoint scratch
-        and the round is already prepared."""
+        The selection and master groups overlap only the re-rotation, which uses no
+        scratch; the library orders both streams after the round's table upload."""
         c = self.cfg.check_layer
         main = self.stream
         self.rerotate(kc[c:c + 1], vc[c:c + 1], c, c + 1)

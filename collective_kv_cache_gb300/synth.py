@@ -443,3 +443,58 @@ def selected_noise(rnd: Round, sel: np.ndarray, layers=None, seed: Optional[int]
 def add_noise_bf16(base_bits: np.ndarray, noise: np.ndarray) -> np.ndarray:
     """bf16(float32(base) + noise), round to nearest even: a synthetic 'recomputed' value."""
     return f32_to_bf16_bits(bf16_bits_to_f32(base_bits) + noise)
+
+
+# ---------------------------------------------------------------- synthetic recompute on the host
+# The recomputed K/V the workloads describe (reused value + the generator's noise), built
+# from a host copy of a pool. Only array layout and the noise model: positions come from
+# the caller's block offsets.
+def token_layout(block_len):
+    """Canonical start of each block, and the block and local index of each token."""
+    bl = np.asarray(block_len, dtype=np.int64)
+    start = np.concatenate([[0], np.cumsum(bl)[:-1]])
+    tok_block = np.repeat(np.arange(len(bl)), bl)
+    u = np.arange(int(bl.sum())) - start[tok_block]
+    return start, tok_block, u
+
+
+def positions(off: np.ndarray, block_len) -> np.ndarray:
+    """[N][S]: prompt position of canonical token t in agent i, from block offsets off[N][M]."""
+    _, tb, u = token_layout(block_len)
+    return off[:, tb] + u[None, :]
+
+
+def gather_rows(pool: np.ndarray, block_table: np.ndarray, P: int, agent: int, layer: int,
+                kv: int, pos: np.ndarray) -> np.ndarray:
+    """Rows of one agent's paged cache (host array [L][2][pages][P][H][D]) at prompt
+    positions pos -> [len(pos)][E]."""
+    pages = block_table[agent, pos // P]
+    assert (pages >= 0).all()
+    rows = pool[layer, kv, pages, pos % P]
+    return rows.reshape(len(pos), pool.shape[4] * pool.shape[5])
+
+
+def recompute_check(cfg: RoundConfig, rnd: Round, pos: np.ndarray, pool: np.ndarray) -> np.ndarray:
+    """Recomputed K at the check layer, [N][S][E] bf16 bits: reused K + check-layer noise."""
+    noise = check_noise(rnd)
+    out = np.empty((cfg.n_agents, cfg.n_shared, cfg.elems), dtype=np.uint16)
+    for i in range(cfg.n_agents):
+        reused = gather_rows(pool, rnd.block_table, cfg.page_size, i, cfg.check_layer, 0, pos[i])
+        out[i] = add_noise_bf16(reused, noise[i])
+    return out
+
+
+def recompute_selected(cfg: RoundConfig, rnd: Round, pos: np.ndarray, pool: np.ndarray,
+                       vc: np.ndarray, sel: np.ndarray):
+    """Recomputed K (agent frame, from the pool) and V (from the canonical V) at the
+    selected tokens of every layer: [N][L][k][E] bf16 bits each."""
+    nk, nv = selected_noise(rnd, sel)
+    N, L, k, E = cfg.n_agents, cfg.n_layers, sel.shape[1], cfg.elems
+    kf = np.empty((N, L, k, E), dtype=np.uint16)
+    vf = np.empty((N, L, k, E), dtype=np.uint16)
+    for i in range(N):
+        for l in range(L):
+            reused = gather_rows(pool, rnd.block_table, cfg.page_size, i, l, 0, pos[i, sel[i]])
+            kf[i, l] = add_noise_bf16(reused, nk[i, l])
+            vf[i, l] = add_noise_bf16(vc[l, sel[i]], nv[i, l])
+    return kf, vf

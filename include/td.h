@@ -22,9 +22,29 @@
  *     ordinary host memory. Each argument says which it is. All memory is owned by the
  *     caller except the context's private workspace.
  *   - bf16 tensors are raw 16-bit patterns, row-major. E = n_kv_heads * head_dim.
- *   - S = sum of block_len (shared tokens). nb = ceil(S / 16) diff blocks.
- *   - Calls are asynchronous on `stream` (a cudaStream_t) unless stated otherwise. Calls
- *     that share a context must be ordered (one stream, or the caller's events).
+ *   - S = sum of block_len (shared tokens). B = td_shape.diff_block tokens per diff block
+ *     (16 or 32) and nb = ceil(S / B) diff blocks.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t) unless stated otherwise.
+ *   - Concurrency on one context. A context is used by one host thread at a time. Its
+ *     calls may be issued on several streams:
+ *       . the round's tables (offsets, RoPE, token blocks) are the context's and shared:
+ *         a stream's first call after they are uploaded is ordered after the upload, and
+ *         a call with a different round waits on the device (events on the other streams,
+ *         no host blocking) until every earlier call that reads the old tables has
+ *         finished before it replaces them;
+ *       . beyond the tables, calls of one group share scratch, so at most one call of
+ *         each group may be in flight at a time (order them: one stream, or events):
+ *           selection  td_check_select, td_check_select_group
+ *           master     td_pick_master, td_pick_master_min_deviation
+ *           encode     td_diff_encode
+ *           attention  td_fused_attention, td_paged_attention
+ *         td_rerotate_batched, td_fused_restore and td_materialise_mirror use no scratch.
+ *       Calls of different groups may overlap: for example td_check_select and
+ *       td_pick_master on one stream while td_rerotate_batched of other layers runs on
+ *       another. Data the caller passes (pool, store, selection) is the caller's to order.
+ *     Inside a stream capture nothing is tracked and a change of round is refused
+ *     (TD_ERR_INVALID_ARG): make a call with the round, and let it finish, before
+ *     capturing calls that use it.
  *   - Host validation runs first; an invalid argument returns TD_ERR_INVALID_ARG and
  *     launches nothing. A CUDA launch or copy failure returns TD_ERR_CUDA.
  *   - Faults found on the device never trap: the offending write is skipped and a bit
@@ -47,18 +67,19 @@ typedef enum td_status {
   TD_ERR_CAPACITY = 3,       /* diff store too small (see td_diff_encode) */
   TD_ERR_UNMAPPED_PAGE = 4,  /* a block-table entry was -1 or >= num_pages */
   TD_ERR_NONFINITE = 5,      /* a key deviation was NaN or infinite */
-  TD_ERR_DEVICE_TIMEOUT = 6, /* reserved: no kernel of this library waits on another */
+  TD_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait on its own copies ran out */
   TD_ERR_SCRATCH_LIMIT = 7   /* sizes exceed the fixed scratch of td_check_select_noalloc */
 } td_status;
 
 /* Model shape. head_dim must be a multiple of 16 (RoPE pairs element f with f + D/2 and
- * the kernels move 8 elements per 16-byte vector); diff_block must be 16. */
+ * the kernels move 8 elements per 16-byte vector); diff_block is 16 or 32 (a 32-token diff
+ * block is one 32-token page: the pages' "diff block = page size" reading). */
 typedef struct td_shape {
   int32_t n_layers;
   int32_t n_kv_heads;
   int32_t head_dim;
   int32_t page_size;    /* tokens per KV page, >= 1 */
-  int32_t diff_block;   /* tokens per diff block on the canonical axis: 16 */
+  int32_t diff_block;   /* tokens per diff block on the canonical axis: 16 or 32 */
   double rope_theta;    /* RoPE base, e.g. 1e6 for Qwen2.5 */
 } td_shape;
 
@@ -94,7 +115,7 @@ typedef struct td_paged {
  *   rowptr              int64 [N*nl + 1]      CSR rows, row = agent*nl + (layer-layer_begin)
  *   block_idx           int32 [capacity]      diff block index b of each record, ascending
  *                                             within a row
- *   val_k, val_v        bf16 [capacity][16][E] the Mirror's whole block; tokens past S are 0
+ *   val_k, val_v        bf16 [capacity][B][E] the Mirror's whole block; tokens past S are 0
  *   slot                int32 [N*nl*nb]       record of (agent, layer, block), or -1
  *   capacity_blocks     records the value arrays can hold
  * The Master's rows are empty. The arrays may also live in page-locked host memory that
@@ -163,7 +184,7 @@ td_status td_check_select(td_ctx* ctx, const td_round* round, int32_t check_laye
 
 /* Stage 3a - Master choice ([R] Summary Method (3): keep the agent with the smallest
  * deviation dense; §3c A2: chosen by a deviation score so the diffs are sparsest).
- * mask_i = diff blocks (16 tokens) holding a token of sel_i; cost(m) = sum over i != m of
+ * mask_i = diff blocks (B tokens) holding a token of sel_i; cost(m) = sum over i != m of
  * |mask_i OR mask_m| (the number of diff blocks per layer the Mirrors can need);
  * master = argmin, ties to the lower index.
  *   sel          DEVICE int32 [N][k]
@@ -230,7 +251,7 @@ td_status td_diff_encode(td_ctx* ctx, const td_round* round, const int32_t* mast
  * into the Master's data in flight and RoPE is recovered, with no dense Mirror; §2a
  * "Fused restore: Master chunk + diff -> paged KV"; §3d). For each listed agent a, layer
  * l in [layer_begin, layer_end) (inside the store's range) and token t: source = a's
- * diff record for (l, t / 16) if present, else the Master; pool K at a's position of t =
+ * diff record for (l, t / B) if present, else the Master; pool K at a's position of t =
  * bf16(R(off) source K) when frame == 0, or source K unchanged when frame == 1; pool V =
  * source V. Rounding as in stage 1.
  *   agents  HOST int32 [n_list], each in [0, N) */
@@ -248,9 +269,14 @@ td_status td_fused_restore(td_ctx* ctx, const td_round* round, const td_diff_sto
  * deviations and an error word - is one fixed array in device memory (about 4.5 MiB),
  * held by every GPU that loads the library until the process exits.
  * Limits: N <= 256, M <= 256, N*M <= 16384, S <= 65536, N*S <= 1048576; larger rounds
- * return TD_ERR_SCRATCH_LIMIT before anything is launched.
+ * return TD_ERR_SCRATCH_LIMIT before anything is launched. diff_block may be 16 or 32 (the
+ * selection does not depend on it).
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture. Every call
+ * with that device current; make that first call before any stream capture. After a
+ * device reset the next call looks the address up again (the device has a new context).
+ * The round's host arrays are copied to the array on `stream`: when they are page-locked
+ * the copy may run after the call returns, so keep them unchanged until the stream has
+ * passed the call (pageable arrays are read before the call returns). Every call
  * reuses the same array: calls whose work can overlap on the GPU (different streams
  * without ordering between them, or several host threads) race on it and must be
  * serialized by the caller. The error word is cleared at the start of each call.

@@ -15,28 +15,9 @@ import oracle as _oracle
 from collective_kv_cache_gb300 import synth
 
 
-def token_layout(block_len):
-    """canonical start of each block, and block / local index of each canonical token"""
-    bl = np.asarray(block_len, dtype=np.int64)
-    start = np.concatenate([[0], np.cumsum(bl)[:-1]])
-    tok_block = np.repeat(np.arange(len(bl)), bl)
-    u = np.arange(int(bl.sum())) - start[tok_block]
-    return start, tok_block, u
-
-
-def positions(off: np.ndarray, block_len) -> np.ndarray:
-    """[N][S]: prompt position of canonical token t in agent i."""
-    _, tb, u = token_layout(block_len)
-    return off[:, tb] + u[None, :]
-
-
-def gather_rows(pool: np.ndarray, block_table: np.ndarray, P: int, agent: int, layer: int,
-                kv: int, pos: np.ndarray) -> np.ndarray:
-    """Rows of one agent's paged cache at prompt positions pos -> [len(pos)][E]."""
-    pages = block_table[agent, pos // P]
-    assert (pages >= 0).all()
-    rows = pool[layer, kv, pages, pos % P]          # [n][H][D]
-    return rows.reshape(len(pos), pool.shape[4] * pool.shape[5])
+token_layout = synth.token_layout
+positions = synth.positions
+gather_rows = synth.gather_rows
 
 
 @dataclasses.dataclass
@@ -89,28 +70,12 @@ def fill_history(cfg: synth.RoundConfig, rnd: synth.Round, pool: np.ndarray,
 
 def fresh_check(ch: Chain, pool: np.ndarray) -> np.ndarray:
     """Synthetic recomputed K at the check layer: reused K + check-layer noise."""
-    cfg, rnd = ch.cfg, ch.rnd
-    noise = synth.check_noise(rnd)
-    out = np.empty((cfg.n_agents, cfg.n_shared, cfg.elems), dtype=np.uint16)
-    for i in range(cfg.n_agents):
-        reused = gather_rows(pool, rnd.block_table, cfg.page_size, i, cfg.check_layer, 0, ch.pos[i])
-        out[i] = synth.add_noise_bf16(reused, noise[i])
-    return out
+    return synth.recompute_check(ch.cfg, ch.rnd, ch.pos, pool)
 
 
 def fresh_selected(ch: Chain, pool: np.ndarray, sel: np.ndarray):
     """Synthetic recomputed K (agent frame) and V at the selected tokens of every layer."""
-    cfg, rnd = ch.cfg, ch.rnd
-    nk, nv = synth.selected_noise(rnd, sel)
-    N, L, k, E = cfg.n_agents, cfg.n_layers, sel.shape[1], cfg.elems
-    kf = np.empty((N, L, k, E), dtype=np.uint16)
-    vf = np.empty((N, L, k, E), dtype=np.uint16)
-    for i in range(N):
-        for l in range(L):
-            reused = gather_rows(pool, rnd.block_table, cfg.page_size, i, l, 0, ch.pos[i, sel[i]])
-            kf[i, l] = synth.add_noise_bf16(reused, nk[i, l])
-            vf[i, l] = synth.add_noise_bf16(ch.vc[l, sel[i]], nv[i, l])
-    return kf, vf
+    return synth.recompute_selected(ch.cfg, ch.rnd, ch.pos, pool, ch.vc, sel)
 
 
 def run_oracle_chain(ch: Chain, restore: bool = True, orc=None, frame: int = 0) -> Chain:

@@ -252,6 +252,86 @@ def test_overlapped_round_matches_oracle():
     assert s == 0 and bits == 0
 
 
+def test_round_changes_on_a_shared_context_across_streams():
+    """Rounds A, B, A through one context, each with its selection and master on a side
+    stream overlapped with the re-rotation; B on streams of its own. Nothing synchronizes
+    the host between them: the library must order each stream after the round's table
+    upload and hold each upload until the work that reads the previous tables is done.
+    Every round's outputs are the oracle's, bit for bit."""
+    R = _R()
+    cfg = synth.qwen7b().replace(n_layers=4, check_layer=2)
+    chains = [rk.run_oracle_chain(rk.make_inputs(cfg, seed)) for seed in (501, 502)]
+    assert not np.array_equal(chains[0].rnd.perm, chains[1].rnd.perm)
+    streams = [(torch.cuda.current_stream(), torch.cuda.Stream()),
+               (torch.cuda.Stream(), torch.cuda.Stream())]
+    runners, inputs, pools = [], [], []
+    ctx = None
+    for x, ch in enumerate(chains):
+        rr = R.RoundRunner(cfg, ch.rnd.block_len, ch.rnd.hist_len, ch.rnd.perm,
+                           ch.rnd.block_table, ch.rnd.num_pages, stream=streams[x][0],
+                           pool_fill=0x2222, ctx=ctx)
+        ctx = rr.ctx
+        rr.alloc_store(int(ch.cost[ch.master]) * cfg.n_layers)
+        dev = lambda a: R.to_device_bf16(a, "cuda")
+        inputs.append((dev(ch.kc), dev(ch.vc), dev(ch.k_fresh), dev(ch.k_fresh_sel),
+                       dev(ch.v_fresh_sel)))
+        pool_o = oracle.new_pool(cfg, ch.rnd.num_pages, fill=0x2222)
+        assert oracle.get().fused_restore(cfg, ch.desc, ch.master, ch.store,
+                                          np.arange(cfg.n_agents), pool_o, ch.rnd.num_pages,
+                                          ch.rnd.block_table) == 0
+        runners.append(rr)
+        pools.append(pool_o)
+    torch.cuda.synchronize()
+    for x in (0, 1, 0):
+        rr = runners[x]
+        rr.round_step(*inputs[x], list(range(cfg.n_agents)), streams[x][1], torch.cuda.Event(),
+                      torch.cuda.Event())
+    torch.cuda.synchronize()
+    for rr, ch, pool_o in zip(runners, chains, pools):
+        assert int(rr.master_t.item()) == ch.master
+        assert np.array_equal(rr.sel_t.cpu().numpy(), ch.sel)
+        nnz = ch.store["nnz"]
+        assert np.array_equal(rr.store_t["rowptr"].cpu().numpy(), ch.store["rowptr"])
+        assert np.array_equal(R.bits_of(rr.store_t["val_k"][:nnz]), ch.store["val_k"])
+        assert np.array_equal(R.bits_of(rr.store_t["val_v"][:nnz]), ch.store["val_v"])
+        assert np.array_equal(R.bits_of(rr.pool_t), pool_o)
+    s, bits = runners[0].get_error()
+    assert s == 0 and bits == 0
+
+
+def test_encode_reads_inputs_written_just_before_it():
+    """The encode's main kernel reads the canonical rows before its dependency wait (it is
+    scheduled only once the prep kernel has waited for everything earlier). Inputs written
+    by a torch kernel on the same stream right before td_diff_encode, with no
+    synchronization, must be the ones encoded: the store is the oracle's, bit for bit."""
+    R = _R()
+    cfg = synth.qwen7b().replace(n_layers=3)
+    ch = rk.run_oracle_chain(rk.make_inputs(cfg))
+    rr = _runner(cfg, ch)
+    sel_t = torch.from_numpy(ch.sel).cuda()
+    m = rr.pick_master(sel_t)
+    rr.alloc_store(rr.candidate_bound(m))
+    kc_true, vc_true = R.to_device_bf16(ch.kc, "cuda"), R.to_device_bf16(ch.vc, "cuda")
+    kfs, vfs = R.to_device_bf16(ch.k_fresh_sel, "cuda"), R.to_device_bf16(ch.v_fresh_sel, "cuda")
+    kc = torch.full_like(kc_true, 7.0)
+    vc = torch.full_like(vc_true, -3.0)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(rr.stream):
+        kc.copy_(kc_true)
+        vc.copy_(vc_true)
+    nnz = rr.diff_encode(kc, vc, kfs, vfs, sel=sel_t)
+    torch.cuda.synchronize()
+    t = rr.store_t
+    assert nnz == ch.store["nnz"]
+    assert np.array_equal(R.bits_of(t["master_k"]), ch.store["master_k"])
+    assert np.array_equal(R.bits_of(t["master_v"]), ch.store["master_v"])
+    assert np.array_equal(t["rowptr"].cpu().numpy(), ch.store["rowptr"])
+    assert np.array_equal(R.bits_of(t["val_k"][:nnz]), ch.store["val_k"])
+    assert np.array_equal(R.bits_of(t["val_v"][:nnz]), ch.store["val_v"])
+    s, bits = rr.get_error()
+    assert s == 0 and bits == 0
+
+
 def test_store_in_host_memory():
     """The store may live in page-locked host memory that the GPU addresses directly
     (NVLink-C2C on GB300): encode writes it there and restore reads it back; both match
@@ -285,8 +365,13 @@ def test_store_in_host_memory():
     assert np.array_equal(host["rowptr"].numpy(), ch.store["rowptr"])
     assert np.array_equal(host["val_k"][:nnz].view(torch.int16).numpy().view(np.uint16),
                           ch.store["val_k"])
-    assert np.array_equal(host["master_v"].view(torch.int16).numpy().view(np.uint16),
-                          ch.store["master_v"])
+    bits16 = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(bits16(host["master_k"]), ch.store["master_k"])
+    assert np.array_equal(bits16(host["master_v"]), ch.store["master_v"])
+    assert np.array_equal(host["block_idx"][:nnz].numpy(), ch.store["idx"])
+    assert np.array_equal(bits16(host["val_v"][:nnz]), ch.store["val_v"])
+    from tests.gpu_chain import _check_slots
+    _check_slots(host["slot"].numpy(), ch.store, N, L, rr.nb)
     rr.fused_restore(list(range(N)))
     torch.cuda.synchronize()
     assert np.array_equal(R.bits_of(rr.pool_t), pool_o)

@@ -1,6 +1,8 @@
 """td_check_select_noalloc: the selection entry point for callers that may not allocate
-device memory. It must give exactly what td_check_select gives (same selection, same k)
-on consecutive calls that reuse its fixed scratch, and refuse rounds that do not fit.
+device memory (code under an allocator that forbids cudaMalloc, or a process whose device
+footprint must stay fixed after start-up). On consecutive calls that reuse its fixed
+scratch it must give exactly the oracle's selection and exactly what td_check_select gives
+on the same inputs, and it must refuse rounds that do not fit its scratch.
 
 Collected last on purpose, so that a run that stops at the first failure has run every
 other test first; it also passes on its own in a fresh process.
@@ -12,7 +14,9 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import oracle
 from collective_kv_cache_gb300 import synth
+from tests import roundkit as rk
 
 pytestmark = pytest.mark.gpu
 
@@ -27,47 +31,53 @@ def lib():
     return td
 
 
-def _prepared_round(cfg, td):
-    """A round re-rotated into its pool by the context path, the synthetic recomputed K at
-    the check layer, and the context path's selection."""
+def _oracle_round(cfg):
+    """The oracle's re-rotated pool, recomputed K at the check layer and selection, with the
+    same pool and K on the device."""
     from collective_kv_cache_gb300 import runner as R
-    rnd = synth.make_round(cfg)
-    kc, vc = synth.canonical_kv(cfg)
+    orc = oracle.get()
+    ch = rk.make_inputs(cfg)
+    rnd = ch.rnd
+    pool_o = oracle.new_pool(cfg, rnd.num_pages)
+    assert orc.rerotate(cfg, ch.desc, ch.kc, ch.vc, pool_o, rnd.num_pages, rnd.block_table) == 0
+    k_fresh = rk.fresh_check(ch, pool_o)
+    st, sel, _ = orc.check_select(cfg, ch.desc, pool_o, rnd.num_pages, rnd.block_table, k_fresh)
+    assert st == 0
     rr = R.RoundRunner(cfg, rnd.block_len, rnd.hist_len, rnd.perm, rnd.block_table,
                        rnd.num_pages)
-    rr.rerotate(R.to_device_bf16(kc, "cuda"), R.to_device_bf16(vc, "cuda"))
-    pos = rr.positions()
-    noise = torch.from_numpy(synth.check_noise(rnd)).cuda()
-    kf = torch.stack([(rr.gather(i, cfg.check_layer, 0, pos[i]).float() + noise[i])
-                      .to(torch.bfloat16) for i in range(cfg.n_agents)])
-    sel_ref = rr.check_select(kf).clone()
-    torch.cuda.synchronize()
-    return rr, kf, sel_ref
+    rr.pool_t.copy_(R.to_device_bf16(pool_o, "cuda").view(rr.pool_t.shape))
+    kf = R.to_device_bf16(k_fresh, "cuda")
+    return rr, kf, sel
 
 
-def _mini():
-    return synth.RoundConfig(
-        name="mini", n_agents=4, n_layers=3, n_kv_heads=2, head_dim=64, page_size=16,
-        block_lens=(20, 37, 16, 9), hist_range=(0, 45), check_layer=1, recompute_pct=15,
-        seed=77)
+def _mini(**kw):
+    base = dict(name="mini", n_agents=4, n_layers=3, n_kv_heads=2, head_dim=64, page_size=16,
+                block_lens=(20, 37, 16, 9), hist_range=(0, 45), check_layer=1,
+                recompute_pct=15, seed=77)
+    base.update(kw)
+    return synth.RoundConfig(**base)
 
 
-def test_noalloc_matches_context_path_on_consecutive_calls(lib):
+def test_noalloc_matches_oracle_and_context_path_on_consecutive_calls(lib):
     td = lib
-    rounds = [_prepared_round(_mini(), td),
-              _prepared_round(synth.qwen7b().replace(n_layers=3), td)]
-    # A, B, A: the second and third calls find the previous call's contents in the scratch
-    for idx in (0, 1, 0):
-        rr, kf, sel_ref = rounds[idx]
+    rounds = [_oracle_round(_mini()),
+              _oracle_round(synth.qwen7b().replace(n_layers=3)),
+              _oracle_round(_mini(diff_block=32, page_size=32, seed=78))]
+    # A, B, C, A: later calls find the previous call's contents in the scratch
+    for idx in (0, 1, 2, 0):
+        rr, kf, sel_orc = rounds[idx]
         cfg = rr.cfg
-        sel = torch.full_like(sel_ref, -7)
+        sel = torch.full(sel_orc.shape, -7, dtype=torch.int32, device="cuda")
         s, k, bits = td.td_check_select_noalloc(td.make_shape(cfg), rr.round, cfg.check_layer,
                                                 rr.pool, kf.data_ptr(), cfg.recompute_pct,
                                                 sel.data_ptr(), rr.s)
         assert s == td.TD_OK and bits == 0, (s, bits)
-        assert k == sel_ref.shape[1]
+        assert k == sel_orc.shape[1]
         torch.cuda.synchronize()
-        assert torch.equal(sel, sel_ref), f"selection differs on round {idx}"
+        assert np.array_equal(sel.cpu().numpy(), sel_orc), f"round {idx}: differs from the oracle"
+        sel_ctx = rr.check_select(kf)
+        torch.cuda.synchronize()
+        assert torch.equal(sel, sel_ctx), f"round {idx}: differs from td_check_select"
 
 
 def test_noalloc_rejects_rounds_beyond_its_scratch(lib):
