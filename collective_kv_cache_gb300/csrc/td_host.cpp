@@ -51,7 +51,6 @@ struct td_ctx {
   // scratch
   float* d_dev = nullptr;           // [max_agents * max_shared]
   uint32_t* d_sel_hist = nullptr;   // [max_agents * kSelHistBins] selection histograms (zero)
-  int32_t* d_sel_done = nullptr;    // [max_agents] selection counters (zero)
   float* d_gdev = nullptr;          // [max_shared] group deviation (variant)
   double* d_score = nullptr;        // [max_agents] deviation totals (variant)
   uint32_t* d_selbits = nullptr;    // [max_agents * max_nb]
@@ -91,7 +90,6 @@ void free_ctx(td_ctx* c) {
   cudaFree(c->d_blk_start);
   cudaFree(c->d_dev);
   cudaFree(c->d_sel_hist);
-  cudaFree(c->d_sel_done);
   cudaFree(c->d_gdev);
   cudaFree(c->d_score);
   cudaFree(c->d_selbits);
@@ -549,7 +547,6 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   chk(cudaMalloc(&c->d_blk_start, static_cast<size_t>(max_blocks) * 4));
   chk(cudaMalloc(&c->d_dev, NS * 4));
   chk(cudaMalloc(&c->d_sel_hist, static_cast<size_t>(max_agents) * kSelHistBins * 4));
-  chk(cudaMalloc(&c->d_sel_done, static_cast<size_t>(max_agents) * 4));
   chk(cudaMalloc(&c->d_gdev, static_cast<size_t>(max_shared) * 4));
   chk(cudaMalloc(&c->d_score, static_cast<size_t>(max_agents) * 8));
   chk(cudaMalloc(&c->d_selbits, static_cast<size_t>(max_agents) * max_nb * 4));
@@ -572,7 +569,6 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   if (e == cudaSuccess) e = cudaMemset(c->d_ints, 0, 8 * sizeof(int32_t));
   if (e == cudaSuccess)
     e = cudaMemset(c->d_sel_hist, 0, static_cast<size_t>(max_agents) * kSelHistBins * 4);
-  if (e == cudaSuccess) e = cudaMemset(c->d_sel_done, 0, static_cast<size_t>(max_agents) * 4);
   if (e != cudaSuccess) {
     free_ctx(c);
     return TD_ERR_CUDA;
@@ -648,7 +644,7 @@ td_status td_check_select(td_ctx* c, const td_round* r, int32_t check_layer,
   float* dev = dev_out ? dev_out : c->d_dev;
   const RoundDev rd = round_dev(c);
   if (launch_check_select(c->g, rd, pd, check_layer, static_cast<const uint16_t*>(k_fresh), dev,
-                          k, sel, c->d_sel_hist, c->d_sel_done, c->d_err, st) != cudaSuccess)
+                          k, sel, c->d_sel_hist, c->d_err, st) != cudaSuccess)
     return TD_ERR_CUDA;
   return note_use(c, st);
 }

@@ -99,13 +99,12 @@ cudaError_t launch_deviation(const Geom& g, const RoundDev& rd, const PoolDev& p
 cudaError_t launch_select(const float* dev, int N, int S, int k, int32_t* sel,
                           cudaStream_t st);
 
-// Deviations and the per-agent top-k in one launch. hist: [N][4096] first-digit counts and
-// done: [N] counters, both zero between calls (the kernel leaves them zero).
+// Deviations, then the per-agent top-k (two launches). hist: [N][4096] first-digit counts,
+// zero between calls (the top-k leaves them zero).
 constexpr int kSelHistBins = 4096;
 cudaError_t launch_check_select(const Geom& g, const RoundDev& rd, const PoolDev& pool,
                                 int check_layer, const uint16_t* k_fresh, float* dev, int k,
-                                int32_t* sel, uint32_t* hist, int* done, uint32_t* err,
-                                cudaStream_t st);
+                                int32_t* sel, uint32_t* hist, uint32_t* err, cudaStream_t st);
 
 // gmask: [N][nbw] scratch; done: a counter that is zero between calls.
 cudaError_t launch_pick_master(const int32_t* sel, int N, int S, int B, int k, int64_t* cost,
