@@ -14,12 +14,14 @@
 // Two launches, the second a programmatic dependent launch of the first:
 //   dev_kernel   the round's N*S (agent, token) pairs are cut into one equal range per
 //                resident CTA (one wave, two CTAs an SM), so every SM moves the same
-//                bytes. Each warp starts the loads of its first recomputed rows, the CTA
-//                looks up the prompt position and pool row of each of its tokens, then each
-//                warp takes every eighth token with 8 KiB of rows in flight (16-byte loads,
-//                not kept in L1). The deviations go to `dev`; the first 12 bits of each key
-//                are counted in the agent's histogram.
-//   topk_kernel  one 256-thread CTA per agent: the histogram gives the threshold's first
+//                bytes. Each warp takes every eighth token of the range through a ring of
+//                12 KiB of shared memory filled by cp.async (16-byte copies, each lane its
+//                own cells, refilled the moment a token is consumed). The recomputed rows
+//                of the ring's first tokens need no lookup and are in flight first; then
+//                the CTA looks up the pool row of each of its tokens (its prompt position
+//                from the round's table, then the block table). The deviations go to
+//                `dev`; the first 12 bits of each key are counted in the agent's histogram.
+//   topk_kernel  one 512-thread CTA per agent: the histogram gives the threshold's first
 //                digit, two 10-bit passes over the agent's keys (staged in shared memory)
 //                give the rest, and warp ballots in token order write the selection
 //                ascending. It clears the histogram for the next call.
@@ -27,8 +29,8 @@
 
 namespace td {
 
-// ---- the selection of one agent (256 threads)
-constexpr int kSelThreads = 256;
+// ---- the selection of one agent (one 512-thread CTA)
+constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelBins2 = 1024;        // second and third digits: bits 19..10 and 9..0
 constexpr int kSelKeysSmem = 16384;    // keys an agent's selection stages (64 KiB)
@@ -45,14 +47,16 @@ __device__ __forceinline__ T block_excl_scan(T x, T* s_warp, T* total) {
   }
   if (lane == 31) s_warp[wid] = incl;
   __syncthreads();
-  T before = 0, tot = 0;
+  // every warp scans the warp totals itself: lane q holds the total of warp q
+  const T w = lane < kSelWarps ? s_warp[lane] : T(0);
+  T wincl = w;
 #pragma unroll
-  for (int q = 0; q < kSelWarps; ++q) {
-    const T w = s_warp[q];
-    before += q < wid ? w : T(0);
-    tot += w;
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_up_sync(0xFFFFFFFFu, wincl, o);
+    if (lane >= o) wincl += y;
   }
-  *total = tot;
+  const T before = __shfl_sync(0xFFFFFFFFu, wincl - w, wid);
+  *total = __shfl_sync(0xFFFFFFFFu, wincl, kSelWarps - 1);
   __syncthreads();   // s_warp may be rewritten by the next scan
   return before + incl - x;
 }
@@ -105,7 +109,7 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const bool staged = s_keys && S <= kSelKeysSmem;
   if (staged) {
-    constexpr int kBatch = 16;                        // a thread's loads in flight together
+    constexpr int kBatch = 4;                         // a thread's loads in flight together
     for (int t0 = 0; t0 < S; t0 += kSelThreads * kBatch) {
       uint32_t v[kBatch];
 #pragma unroll
@@ -121,7 +125,7 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
     }
   }
   auto key_at = [&](int t) { return staged ? s_keys[t] : __ldcg(keys_g + t); };
-  constexpr int kPer1 = kSelHistBins / kSelThreads;   // 16
+  constexpr int kPer1 = kSelHistBins / kSelThreads;   // 8
   uint32_t h1[kPer1];
   if (hist_g) {
     uint4* hp = reinterpret_cast<uint4*>(hist_g + kSelHistBins - kPer1 * (tid + 1));
@@ -161,17 +165,12 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
   // bin (need_eq = 0) and the remaining digits are not needed.
   int64_t T = (static_cast<int64_t>(d1) << 20) - 1;
   int need_eq = 0;
-  constexpr int kPer2 = kSelBins2 / kSelThreads;   // 4
+  constexpr int kPer2 = kSelBins2 / kSelThreads;   // 2
   if (s_d1[1] != s_d1[2]) {
-    // digit 2 (bits 19..10) among the keys of bin d1 (tied keys are common: one atomic per
-    // distinct bin of a warp)
-    for (int t0 = 0; t0 < S; t0 += kSelThreads) {   // uniform trip count
-      const int t = t0 + tid;
-      const uint32_t key = t < S ? key_at(t) : 0u;
-      const unsigned b = t < S && (key >> 20) == d1 ? ((key >> 10) & 1023u) : 0xFFFFFFFFu;
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, b);
-      if (b != 0xFFFFFFFFu && lane == __ffs(peers) - 1)
-        atomicAdd(&s_h2[b], static_cast<unsigned>(__popc(peers)));
+    // digit 2 (bits 19..10) among the keys of bin d1
+    for (int t = tid; t < S; t += kSelThreads) {
+      const uint32_t key = key_at(t);
+      if ((key >> 20) == d1) atomicAdd(&s_h2[(key >> 10) & 1023u], 1u);
     }
     __syncthreads();
     uint32_t h2[kPer2];
@@ -182,13 +181,9 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
     T = (static_cast<int64_t>(p2) << 10) - 1;
     if (s_d2[1] != s_d2[2]) {
       // digit 3 (bits 9..0) among the keys of bin (d1, d2)
-      for (int t0 = 0; t0 < S; t0 += kSelThreads) {
-        const int t = t0 + tid;
-        const uint32_t key = t < S ? key_at(t) : 0u;
-        const unsigned b = t < S && (key >> 10) == p2 ? (key & 1023u) : 0xFFFFFFFFu;
-        const unsigned peers = __match_any_sync(0xFFFFFFFFu, b);
-        if (b != 0xFFFFFFFFu && lane == __ffs(peers) - 1)
-          atomicAdd(&s_h3[b], static_cast<unsigned>(__popc(peers)));
+      for (int t = tid; t < S; t += kSelThreads) {
+        const uint32_t key = key_at(t);
+        if ((key >> 10) == p2) atomicAdd(&s_h3[key & 1023u], 1u);
       }
       __syncthreads();
       uint32_t h3[kPer2];
@@ -237,10 +232,11 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
 }
 
 // ---- dev_kernel
-constexpr int kDevThreads = kSelThreads;
+constexpr int kDevThreads = 256;
 constexpr int kDevWarps = kDevThreads / 32;
 constexpr int kDevCtasPerSm = 2;
-constexpr int kDevMaxTok = 1024;       // (agent, token) pairs per CTA at most
+constexpr int kDevMaxTok = 1024;          // (agent, token) pairs per CTA at most
+constexpr int kDevWarpRing = 12 * 1024;   // bytes of rows a warp has in flight
 
 struct DevArgs {
   Geom g;
@@ -255,45 +251,60 @@ struct DevArgs {
   int per_cta;          // (agent, token) pairs per CTA
 };
 
-// A 16-byte load of data read once: not kept in L1.
-__device__ __forceinline__ uint4 ld_stream16(const uint16_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+// The prompt position of every token of the round (one thread a token).
+__global__ void __launch_bounds__(256) positions_kernel(RoundDev rd, int32_t* pos) {
+  const int64_t total = static_cast<int64_t>(rd.N) * rd.S;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(g / rd.S);
+    const int t = static_cast<int>(g - static_cast<int64_t>(i) * rd.S);
+    const int j = rd.tok_block[t];
+    pos[g] = rd.off[i * rd.M + j] + t - rd.blk_start[j];
+  }
 }
 
-// kVec: 16-byte vectors a lane takes of a row (lane l: vectors l, l + 32, ...); kDepth:
-// tokens a warp has in flight (8 KiB of rows).
-template <int kVec, int kDepth>
+cudaError_t launch_positions(const RoundDev& rd, int32_t* pos, cudaStream_t st) {
+  const int64_t total = static_cast<int64_t>(rd.N) * rd.S;
+  const int64_t blocks = (total + 255) / 256;
+  positions_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(rd,
+                                                                                        pos);
+  return cudaGetLastError();
+}
+
+// kVec: 16-byte vectors a lane takes of a row (lane l: vectors l, l + 32, ...); kSlots:
+// tokens in a warp's ring (both rows of a token in one slot, 12 KiB a warp).
+template <int kVec, int kSlots>
 __global__ void __launch_bounds__(kDevThreads, kDevCtasPerSm) dev_kernel(DevArgs a) {
-  __shared__ int64_t s_row[kDevMaxTok];  // pool row of each token, -1 unmapped
+  __shared__ int64_t s_row[kDevMaxTok];   // pool row of each token, -1 unmapped
   __shared__ uint32_t s_key[kDevMaxTok];
+  extern __shared__ uint4 s_ring[];       // [warp][slot][recomputed, reused][kVec][lane]
   const int S = a.rd.S, M = a.rd.M, E = a.g.E;
   const int64_t total = static_cast<int64_t>(a.rd.N) * S;
   const int64_t g0 = static_cast<int64_t>(blockIdx.x) * a.per_cta;
   const int n = static_cast<int>(min(static_cast<int64_t>(a.per_cta), total - g0));
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nv = E >> 3;                      // 16-byte vectors of a row
-  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  pdl_wait();
-  // the recomputed rows of the warp's first tokens need no lookup: in flight at once
-  uint4 fv[kDepth][kVec], rv[kDepth][kVec];
-  auto load_fresh = [&](int x0) {
+  const int nq = n > wid ? (n - wid + kDevWarps - 1) / kDevWarps : 0;   // this warp's tokens
+  uint4* ring = s_ring + static_cast<size_t>(wid) * kSlots * 2 * kVec * 32;
+  const uint64_t policy = l2_evict_first();   // every row is read once
+  // lane l copies, and later reads, only its own cells: no barrier, only the group waits
+  auto copy_row = [&](int slot, int which, const uint16_t* row) {
 #pragma unroll
-    for (int u = 0; u < kDepth; ++u) {
-      const int x = x0 + u * kDevWarps;
-      const uint16_t* fr = a.kf + (g0 + min(x, n - 1)) * E;
-#pragma unroll
-      for (int r = 0; r < kVec; ++r) {
-        const int v = lane + 32 * r;
-        fv[u][r] = (x < n && v < nv) ? ld_stream16(fr + v * 8) : z;
-      }
-    }
+    for (int r = 0; r < kVec; ++r)
+      if (lane + 32 * r < nv)
+        cp_async16_hint(ring + ((slot * 2 + which) * kVec + r) * 32 + lane,
+                        row + (lane + 32 * r) * 8, policy);
   };
-  load_fresh(wid);
-  // the pool row of every token of the range (all of a thread's loads issued first)
+  auto fresh_row = [&](int q) { return a.kf + (g0 + wid + q * kDevWarps) * E; };
+  auto reused_row = [&](int q) { return a.pool.base + s_row[wid + q * kDevWarps] * E; };
+  pdl_wait();
+  // the recomputed rows of the ring's first tokens need no lookup: in flight at once
+#pragma unroll
+  for (int q = 0; q < kSlots; ++q)
+    if (q < nq) copy_row(q, 0, fresh_row(q));
+  cp_async_commit();
+  // the pool row of every token of the range: its prompt position from the round's table,
+  // then the block table (all of a thread's loads issued first)
   {
     constexpr int kPer = kDevMaxTok / kDevThreads;
     int pos[kPer], ag[kPer];
@@ -302,9 +313,13 @@ __global__ void __launch_bounds__(kDevThreads, kDevCtasPerSm) dev_kernel(DevArgs
       const int x = min(tid + q * kDevThreads, n - 1);
       const int64_t g = g0 + x;
       ag[q] = static_cast<int>(g / S);
-      const int t = static_cast<int>(g - static_cast<int64_t>(ag[q]) * S);
-      const int j = __ldg(a.rd.tok_block + t);
-      pos[q] = __ldg(a.rd.off + ag[q] * M + j) + t - __ldg(a.rd.blk_start + j);
+      if (a.rd.pos) {
+        pos[q] = __ldg(a.rd.pos + g);
+      } else {
+        const int t = static_cast<int>(g - static_cast<int64_t>(ag[q]) * S);
+        const int j = __ldg(a.rd.tok_block + t);
+        pos[q] = __ldg(a.rd.off + ag[q] * M + j) + t - __ldg(a.rd.blk_start + j);
+      }
     }
 #pragma unroll
     for (int q = 0; q < kPer; ++q)
@@ -313,53 +328,61 @@ __global__ void __launch_bounds__(kDevThreads, kDevCtasPerSm) dev_kernel(DevArgs
             pool_row_index(a.pool, ag[q], a.check_layer, 0, pos[q], a.err);
   }
   __syncthreads();
-  // deviations: warp w takes tokens w, w + 8, ..., kDepth of them at a time with all their
-  // loads in flight together
-  for (int x0 = wid; x0 < n; x0 += kDevWarps * kDepth) {   // uniform across the warp
-    if (x0 != wid) load_fresh(x0);
+  // then their reused rows, one group per token: groups complete in order, so token q has
+  // landed when at most kSlots - 1 groups are pending
 #pragma unroll
-    for (int u = 0; u < kDepth; ++u) {
-      const int x = x0 + u * kDevWarps;
-      const int64_t row = x < n ? s_row[x] : -1;
-      const uint16_t* rr = a.pool.base + (row >= 0 ? row : 0) * E;
+  for (int q = 0; q < kSlots; ++q) {
+    if (q < nq && s_row[wid + q * kDevWarps] >= 0) copy_row(q, 1, reused_row(q));
+    cp_async_commit();
+  }
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+  for (int q0 = 0; q0 < nq; q0 += kSlots) {
 #pragma unroll
-      for (int r = 0; r < kVec; ++r) {
-        const int v = lane + 32 * r;
-        rv[u][r] = (row >= 0 && v < nv) ? ld_stream16(rr + v * 8) : z;
-      }
-    }
+    for (int u = 0; u < kSlots; ++u) {
+      const int q = q0 + u;
+      cp_async_wait<kSlots - 1>();
+      if (q < nq) {                           // uniform across the warp
+        const int x = wid + q * kDevWarps;
+        const bool mapped = s_row[x] >= 0;
+        float acc = 0.0f;
 #pragma unroll
-    for (int u = 0; u < kDepth; ++u) {
-      const int x = x0 + u * kDevWarps;
-      float acc = 0.0f;
+        for (int r = 0; r < kVec; ++r) {
+          if (lane + 32 * r < nv) {
+            float fx[8], rx[8];
+            unpack8(ring[((u * 2 + 0) * kVec + r) * 32 + lane], fx);
+            unpack8(mapped ? ring[((u * 2 + 1) * kVec + r) * 32 + lane] : z, rx);
 #pragma unroll
-      for (int r = 0; r < kVec; ++r) {
-        if (lane + 32 * r < nv) {
-          float fx[8], rx[8];
-          unpack8(fv[u][r], fx);
-          unpack8(rv[u][r], rx);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float d = __fsub_rn(fx[q], rx[q]);
-            acc = __fmaf_rn(d, d, acc);
+            for (int e = 0; e < 8; ++e) {
+              const float d = __fsub_rn(fx[e], rx[e]);
+              acc = __fmaf_rn(d, d, acc);
+            }
           }
         }
-      }
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1)
-        acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
-      if (lane == 0 && x < n) {
-        if (s_row[x] < 0) {
-          acc = 0.0f;                         // unmapped: reported, deviation 0
-        } else if (!isfinite(acc)) {
-          atomicOr(a.err, err_bit(TD_ERR_NONFINITE));
+        for (int o = 16; o >= 1; o >>= 1)
+          acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
+        if (lane == 0) {
+          if (!mapped) {
+            acc = 0.0f;                       // unmapped: reported, deviation 0
+          } else if (!isfinite(acc)) {
+            atomicOr(a.err, err_bit(TD_ERR_NONFINITE));
+          }
+          s_key[x] = __float_as_uint(acc);
         }
-        s_key[x] = __float_as_uint(acc);
       }
+      // this lane's cells of the slot are consumed: refill it with token q + kSlots
+      const int qn = q + kSlots;
+      if (qn < nq) {
+        copy_row(u, 0, fresh_row(qn));
+        if (s_row[wid + qn * kDevWarps] >= 0) copy_row(u, 1, reused_row(qn));
+      }
+      cp_async_commit();
     }
   }
+  cp_async_wait<0>();
   __syncthreads();
-  pdl_trigger();   // the next kernel may be scheduled; it waits for this grid to finish
+  pdl_trigger();   // the top-k may be scheduled; it waits for this grid to finish
   // the range's deviations (coalesced) and its keys into the agents' histograms, one
   // atomic per distinct (agent, first digit) of a warp
   for (int x0 = 0; x0 < n; x0 += kDevThreads) {
@@ -378,16 +401,20 @@ __global__ void __launch_bounds__(kDevThreads, kDevCtasPerSm) dev_kernel(DevArgs
   }
 }
 
-template <int kVec, int kDepth>
+template <int kVec, int kSlots>
 static cudaError_t launch_dev_t(const DevArgs& a0, cudaStream_t st) {
+  constexpr size_t kRing = static_cast<size_t>(kDevWarps) * kSlots * 2 * kVec * 32 * 16;
   static int sms[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!sms[dev]) {
+  if (!sms[dev]) {   // the rings pass the default shared-memory window: opt in once
     int n = 0;
-    if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(dev_kernel<kVec, kSlots>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kRing))) != cudaSuccess)
       return e;
     sms[dev] = n;
   }
@@ -399,16 +426,16 @@ static cudaError_t launch_dev_t(const DevArgs& a0, cudaStream_t st) {
   int64_t per = (total + slots - 1) / slots;
   if (per > kDevMaxTok) per = kDevMaxTok;
   a.per_cta = static_cast<int>(per);
-  return launch_after(dev_kernel<kVec, kDepth>, static_cast<unsigned>((total + per - 1) / per),
-                      kDevThreads, 0, st, a);
+  return launch_after(dev_kernel<kVec, kSlots>, static_cast<unsigned>((total + per - 1) / per),
+                      kDevThreads, kRing, st, a);
 }
 
 static cudaError_t launch_dev(const DevArgs& a, cudaStream_t st) {
-  const int nv = a.g.E >> 3;
-  if (nv <= 32) return launch_dev_t<1, 8>(a, st);
-  if (nv <= 64) return launch_dev_t<2, 4>(a, st);
-  if (nv <= 128) return launch_dev_t<4, 2>(a, st);
-  return launch_dev_t<8, 1>(a, st);
+  const int nv = a.g.E >> 3;   // ring slots: kDevWarpRing / (2 rows of kVec * 512 bytes)
+  if (nv <= 32) return launch_dev_t<1, 12>(a, st);
+  if (nv <= 64) return launch_dev_t<2, 6>(a, st);
+  if (nv <= 128) return launch_dev_t<4, 3>(a, st);
+  return launch_dev_t<8, 2>(a, st);
 }
 
 // ---- topk_kernel: one CTA per row of keys already in memory. hist: the rows' first-digit

@@ -50,6 +50,7 @@ struct td_ctx {
 
   // scratch
   float* d_dev = nullptr;           // [max_agents * max_shared]
+  int32_t* d_pos = nullptr;         // [max_agents * max_shared] prompt position of each token
   uint32_t* d_sel_hist = nullptr;   // [max_agents * kSelHistBins] selection histograms (zero)
   float* d_gdev = nullptr;          // [max_shared] group deviation (variant)
   double* d_score = nullptr;        // [max_agents] deviation totals (variant)
@@ -89,6 +90,7 @@ void free_ctx(td_ctx* c) {
   cudaFree(c->d_tok_block);
   cudaFree(c->d_blk_start);
   cudaFree(c->d_dev);
+  cudaFree(c->d_pos);
   cudaFree(c->d_sel_hist);
   cudaFree(c->d_gdev);
   cudaFree(c->d_score);
@@ -257,9 +259,19 @@ td_status prepare_round(td_ctx* c, const td_round* r, cudaStream_t st) {
       (e = cudaMemcpyAsync(c->d_sin, sn, n_off * half * 4, cudaMemcpyHostToDevice, st)) ||
       (e = cudaMemcpyAsync(c->d_tok_block, tokb, S * 4, cudaMemcpyHostToDevice, st)) ||
       (e = cudaMemcpyAsync(c->d_blk_start, bst, M * 4, cudaMemcpyHostToDevice, st)) ||
-      (e = cudaEventRecord(c->stage_done, st)) ||
-      (e = cudaEventRecord(c->tables_ready, st)))
+      (e = cudaEventRecord(c->stage_done, st)))
     return TD_ERR_CUDA;
+  {
+    RoundDev rd{};
+    rd.N = N;
+    rd.M = M;
+    rd.S = static_cast<int>(S);
+    rd.off = c->d_off;
+    rd.tok_block = c->d_tok_block;
+    rd.blk_start = c->d_blk_start;
+    if ((e = launch_positions(rd, c->d_pos, st)) || (e = cudaEventRecord(c->tables_ready, st)))
+      return TD_ERR_CUDA;
+  }
   c->tables_stream = st;
   c->tables_recorded = true;
   for (auto& u : c->users) u.ordered = false;
@@ -288,6 +300,7 @@ RoundDev round_dev(const td_ctx* c) {
   rd.sin_t = c->d_sin;
   rd.tok_block = c->d_tok_block;
   rd.blk_start = c->d_blk_start;
+  rd.pos = c->d_pos;
   return rd;
 }
 
@@ -546,6 +559,7 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   chk(cudaMalloc(&c->d_tok_block, static_cast<size_t>(max_shared) * 4));
   chk(cudaMalloc(&c->d_blk_start, static_cast<size_t>(max_blocks) * 4));
   chk(cudaMalloc(&c->d_dev, NS * 4));
+  chk(cudaMalloc(&c->d_pos, NS * 4));
   chk(cudaMalloc(&c->d_sel_hist, static_cast<size_t>(max_agents) * kSelHistBins * 4));
   chk(cudaMalloc(&c->d_gdev, static_cast<size_t>(max_shared) * 4));
   chk(cudaMalloc(&c->d_score, static_cast<size_t>(max_agents) * 8));

@@ -41,6 +41,7 @@ struct RoundDev {
   const float* sin_t;        // [N*M][D/2]
   const int32_t* tok_block;  // [S] block of each canonical token
   const int32_t* blk_start;  // [M] canonical start of each block
+  const int32_t* pos;        // [N][S] prompt position of each shared token, or nullptr
 };
 
 struct PoolDev {
@@ -91,6 +92,9 @@ int tile_items(const Geom& g);
 cudaError_t launch_rerotate(const Geom& g, const RoundDev& rd, const PoolDev& pool,
                             const uint16_t* kc, const uint16_t* vc, int layer_begin, int nl,
                             uint32_t* err, cudaStream_t st);
+
+// pos[i*S + t] = off[i*M + j(t)] + t - blk_start[j(t)] for the round's tables.
+cudaError_t launch_positions(const RoundDev& rd, int32_t* pos, cudaStream_t st);
 
 cudaError_t launch_deviation(const Geom& g, const RoundDev& rd, const PoolDev& pool,
                              int check_layer, const uint16_t* k_fresh, float* dev,

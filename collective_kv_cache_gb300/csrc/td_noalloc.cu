@@ -198,6 +198,7 @@ extern "C" td_status td_check_select_noalloc(const td_shape* shape, const td_rou
   rd.sin_t = nullptr;
   rd.tok_block = reinterpret_cast<const int32_t*>(base + kOffTok);
   rd.blk_start = reinterpret_cast<const int32_t*>(base + kOffStart);
+  rd.pos = nullptr;   // positions are looked up from the tables above
   PoolDev pd;
   pd.base = static_cast<uint16_t*>(pool->base);
   pd.num_pages = pool->num_pages;
