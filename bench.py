@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 METRIC = "restore+reuse KV GB/s (% of GB300 HBM peak); agent-rounds/sec, 7B shape"
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal (the measured copy peak is the roofline)
-LAUNCHES_PER_STEP = 8    # rerotate 1, deviation + top-k 1, master 1, encode 4, restore 1
+LAUNCHES_PER_STEP = 9    # rerotate 1, deviation 1 + top-k 1, master 1, encode 4, restore 1
 # DRAM bytes (read + write) per launch of the roofline kernels at the benchmarked size, from
 # one ncu capture of these kernels as they are now (dram__bytes_read.sum +
 # dram__bytes_write.sum); set an entry to None when its kernel changes.
@@ -380,8 +380,8 @@ STAGES = ("rerotate", "select", "master", "encode", "restore")
 
 
 def run_overlapped(st, agents, side, ev_check, ev_master, args):
-    """One round with the check layer's selection and the master choice on a second
-    stream, overlapped with the re-rotation of the other layers (--sequential: one
+    """One round with the check layer's selection, the master choice and the encode on a
+    second stream, overlapped with the re-rotation of the other layers (--sequential: one
     stream, stages in order)."""
     if args.sequential:
         run_step(st, agents)
@@ -545,8 +545,8 @@ def bench_ours(args, rank, world, local_rank):
             "gpu_launches": (LAUNCHES_PER_STEP + (0 if args.sequential else
                              (cfg.check_layer > 0) + (cfg.check_layer + 1 < L))) * K,
             "schedule": ("sequential" if args.sequential else
-                         "check layer first; selection and master on a second stream "
-                         "overlapped with the other layers' re-rotation") +
+                         "check layer first; selection, master and encode on a second "
+                         "stream overlapped with the other layers' re-rotation") +
                         ("; one step captured in a CUDA graph, replayed per step"
                          if args.graph else
                          "; kernels launched from the host, each after the previous with "

@@ -21,11 +21,11 @@
 //           waiting for the result. One CTA per block writes the slot map and block
 //           indices of the common case (every candidate kept);
 //   rows    each (agent, layer) row's record count from its flags, one warp a row over
-//           as many CTAs as the rows need; the CTA that finishes last (a self-resetting
-//           counter) takes their prefix sum -> rowptr and decides whether the fix-up runs;
-//   fixup   only when some candidate equalled the Master's block: compacts the slot map
-//           and indices and rewrites the kept blocks whose record moved (recomputed from
-//           the inputs, never copied); otherwise it returns at once.
+//           as many CTAs as the rows need;
+//   fixup   every CTA takes the prefix of the counts (CTA 0 writes rowptr); only when
+//           some candidate equalled the Master's block does it compact the slot map and
+//           indices and rewrite the kept blocks whose record moved (recomputed from the
+//           inputs, never copied); otherwise it returns at once.
 // No Mirror is built densely; in the common case the inputs are read once.
 #include "td_device.cuh"
 
@@ -47,7 +47,6 @@ struct EncArgs {
   int32_t* over;        // bound exceeds capacity
   int64_t* bound;
   int* prep_done;       // CTAs of prep finished (self-resetting)
-  int* rows_done;       // CTAs of the row count finished (self-resetting)
   uint32_t* err;
 };
 
@@ -63,7 +62,6 @@ __device__ void build_candidates(const EncArgs& a, const int32_t* master) {
     }
     s_m = m;
     *a.m_ok = m;
-    *a.sc.need_fixup = 0;
     *a.over = 0;
   }
   __syncthreads();
@@ -150,16 +148,15 @@ __device__ __forceinline__ int64_t cand_place(const EncArgs& a, int i, int li, i
          a.sc.word_prefix[i * nbw + (b >> 5)] + __popc(below);
 }
 
-// Exclusive prefix sum of the per-(agent, layer) record counts -> rowptr (one CTA), in
-// chunks of kPrefixPer rows a thread whose counts are all loaded at once.
+// Exclusive prefix sum of the per-(agent, layer) record counts, in chunks of kPrefixPer
+// rows a thread whose counts are all loaded at once; written to rowptr when `write`.
+// Returns the total. Every thread of the CTA calls it.
 constexpr int kPrefixPer = 8;
 
-__device__ void rows_prefix(const EncArgs& a) {
+__device__ long long rows_prefix(const EncArgs& a, bool write) {
   __shared__ long long wsum[32];
   const int R = a.rd.N * a.nl;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int over = *a.over;
-  const int64_t bound = *a.bound;
   long long carry = 0;
   for (int c0 = 0; c0 < R; c0 += blockDim.x * kPrefixPer) {
     const int r0 = c0 + threadIdx.x * kPrefixPer;
@@ -184,18 +181,18 @@ __device__ void rows_prefix(const EncArgs& a) {
       total += wsum[w];
     }
     long long run = carry + before + incl - local;
+    if (write) {
 #pragma unroll
-    for (int q = 0; q < kPrefixPer; ++q) {
-      if (r0 + q < R) a.store.rowptr[r0 + q] = run;
-      run += cnt[q];
+      for (int q = 0; q < kPrefixPer; ++q) {
+        if (r0 + q < R) a.store.rowptr[r0 + q] = run;
+        run += cnt[q];
+      }
     }
     carry += total;
     __syncthreads();   // wsum is rewritten by the next chunk
   }
-  if (threadIdx.x == 0) {
-    a.store.rowptr[R] = carry;
-    if (!over && carry != bound) *a.sc.need_fixup = 1;
-  }
+  if (write && threadIdx.x == 0) a.store.rowptr[R] = carry;
+  return carry;
 }
 
 // Per-thread items of one half-tile (K or V) of a (layer, 16-token tile) unit.
@@ -478,12 +475,9 @@ constexpr int kRowsThreads = 256;
 constexpr int kRowsPerWarp = 4;   // rows a warp counts at once: their loads are all in flight
 
 __global__ void __launch_bounds__(kRowsThreads) enc_rows_kernel(EncArgs a) {
-  __shared__ int s_last;
   pdl_trigger();
   pdl_wait();
-  // the flags are zeroed by prep whatever the master, so counting starts at once; the
-  // master's check decides only whether the record rows are written
-  const int m_ok = *a.m_ok;
+  // the flags are zeroed by prep whatever the master, so counting needs no check
   const int R = a.rd.N * a.nl, nb = a.rd.nb;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int r0 = (blockIdx.x * nw + wid) * kRowsPerWarp; r0 < R;
@@ -502,29 +496,25 @@ __global__ void __launch_bounds__(kRowsThreads) enc_rows_kernel(EncArgs a) {
       if (lane == 0 && r0 + q < R) a.sc.row_count[r0 + q] = cnt[q];
     }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_last = atomicAdd(a.rows_done, 1) == static_cast<int>(gridDim.x) - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;                        // uniform across the CTA
-  __threadfence();
-  if (threadIdx.x == 0) *a.rows_done = 0;     // ready for the next call
-  if (m_ok >= 0) rows_prefix(a);
 }
 
-// Only when some candidate equalled the Master's block (need_fixup): (1) compact every
-// row's slot map and block indices, warp per row; (2) rewrite each kept block whose
-// final record is not its candidate place, from the inputs. The final record of a kept
-// block is rowptr of its row plus the kept blocks before it, so (2) does not depend on
-// (1). Grid-stride; returns at once in the common case.
+// The row pointers, then the fix-up. Every CTA takes the prefix of the row counts itself,
+// so all agree, without waiting on one another, on whether a candidate equalled the
+// Master's block (the total is below the bound); CTA 0 writes rowptr. Only then: (1)
+// compact every row's slot map and block indices, warp per row; (2) rewrite each kept
+// block whose final record is not its candidate place, from the inputs. The final record
+// of a kept block is rowptr of its row plus the kept blocks before it, so (2) does not
+// depend on (1). Grid-stride; in the common case CTA 0 writes rowptr and all return.
 template <int kItems>
 __global__ void __launch_bounds__(256) enc_fixup_kernel(EncArgs a, int tiles_per_layer) {
   pdl_wait();
-  if (__ldcg(a.sc.need_fixup) == 0) return;
   const int m = *a.m_ok;
-  if (m < 0 || *a.over) return;
+  if (m < 0) return;                          // nothing was encoded: rowptr is not written
+  const long long total = rows_prefix(a, blockIdx.x == 0);
+  if (*a.over || total == *a.bound) return;
+  // every CTA reads rowptr below: it writes the (same) values itself first
+  if (blockIdx.x != 0) rows_prefix(a, true);
+  __syncthreads();
   const int nb = a.rd.nb, R = a.rd.N * a.nl;
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -622,10 +612,9 @@ cudaError_t launch_encode(const Geom& g, const RoundDev& rd, const int32_t* mast
   a.nl = nl;
   a.store = store;
   a.sc = sc;
-  a.m_ok = sc.need_fixup + 1;   // the context lays these ints out after need_fixup
-  a.over = sc.need_fixup + 2;
-  a.prep_done = sc.need_fixup + 3;
-  a.rows_done = sc.need_fixup + 4;
+  a.m_ok = sc.words + 1;
+  a.over = sc.words + 2;
+  a.prep_done = sc.words + 3;
   a.bound = bound_dev;
   a.err = err;
   if (nl <= 0) return cudaSuccess;

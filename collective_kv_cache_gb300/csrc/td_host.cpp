@@ -62,7 +62,7 @@ struct td_ctx {
   int32_t* d_wprefix = nullptr;     // [max_agents * nbw_max + max_agents]
   int64_t* d_aprefix = nullptr;     // [max_agents + 1]
   uint32_t* d_flag = nullptr;       // [max_agents * L * max_nb] flags + [max_agents * L] counts
-  int32_t* d_ints = nullptr;        // need_fixup, m_ok, over, prep_done, rows_done,
+  int32_t* d_ints = nullptr;        // encode's words (unused, m_ok, over, prep_done), spare,
                                     // pick_master's counter, spare
   int64_t* d_bound = nullptr;
   uint32_t* d_err = nullptr;
@@ -780,7 +780,7 @@ td_status td_diff_encode(td_ctx* c, const td_round* r, const int32_t* master,
   sc.flag = c->d_flag;
   sc.row_count = reinterpret_cast<int32_t*>(
       c->d_flag + static_cast<size_t>(c->N) * nl * round_dev(c).nb);
-  sc.need_fixup = c->d_ints;
+  sc.words = c->d_ints;
   sc.nbw = (round_dev(c).nb + 31) / 32;
   cudaError_t e = launch_encode(c->g, round_dev(c), master,
                                 static_cast<const uint16_t*>(k_canon),

@@ -81,7 +81,7 @@ struct EncodeScratch {
   int64_t* agent_prefix;     // [N+1] candidates per layer of agents before i
   uint32_t* flag;            // [N][nl][nb] candidate block differs from the master's
   int32_t* row_count;        // [N][nl] records per row; directly after flag (one memset)
-  int32_t* need_fixup;       // 1 when some candidate equalled the master's block
+  int32_t* words;            // [4]: unused, checked master, over capacity, prep counter
   int nbw;
 };
 

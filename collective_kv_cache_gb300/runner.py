@@ -101,10 +101,11 @@ class RoundRunner:
     def round_step(self, kc, vc, kf, kfs, vfs, agents, side: torch.cuda.Stream, ev_check,
                    ev_master):
         """One round with the check layer's selection overlapped: the check layer is
-        re-rotated first; selection and master choice run on `side` while the other layers
-        are re-rotated on the main stream; encode and restore follow on the main stream.
-        The selection and master groups overlap only the re-rotation, which uses no
-        scratch; the library orders both streams after the round's table upload."""
+        re-rotated first; selection, master choice and the encode (which reads no pages)
+        run on `side` while the other layers are re-rotated on the main stream; the restore
+        follows on the main stream once both are done. Selection, master and encode use
+        their own scratch and re-rotation uses none, so the calls of the two streams may
+        overlap; the library orders both streams after the round's table upload."""
         c = self.cfg.check_layer
         main = self.stream
         self.rerotate(kc[c:c + 1], vc[c:c + 1], c, c + 1)
@@ -112,13 +113,13 @@ class RoundRunner:
         side.wait_event(ev_check)
         self.check_select(kf, stream=side)
         self.pick_master(want_host=False, stream=side)
+        self.diff_encode(kc, vc, kfs, vfs, want_nnz=False, stream=side)
         ev_master.record(side)
         if c > 0:
             self.rerotate(kc[:c], vc[:c], 0, c)
         if c + 1 < self.L:
             self.rerotate(kc[c + 1:], vc[c + 1:], c + 1, self.L)
         main.wait_event(ev_master)
-        self.diff_encode(kc, vc, kfs, vfs, want_nnz=False)
         self.fused_restore(agents, frame=0)
 
     def alloc_store(self, capacity: int, layer_begin=0, layer_end=None):
@@ -143,7 +144,7 @@ class RoundRunner:
         return int(self.cost_t[master].item()) * (layer_end - layer_begin)
 
     def diff_encode(self, kc, vc, kf, vf, sel=None, master_t=None, layer_begin=0,
-                    layer_end=None, want_nnz=True, check=True):
+                    layer_end=None, want_nnz=True, check=True, stream=None):
         layer_end = self.L if layer_end is None else layer_end
         sel = self.sel_t if sel is None else sel
         master_t = self.master_t if master_t is None else master_t
@@ -151,8 +152,8 @@ class RoundRunner:
         return td.td_diff_encode(self.ctx.handle, self.round, master_t.data_ptr(), kc.data_ptr(),
                                  vc.data_ptr(), sel.data_ptr() if k else None, k,
                                  kf.data_ptr() if k else None, vf.data_ptr() if k else None,
-                                 layer_begin, layer_end, self.store, self.s, want_nnz=want_nnz,
-                                 check=check)
+                                 layer_begin, layer_end, self.store, self._s(stream),
+                                 want_nnz=want_nnz, check=check)
 
     def fused_restore(self, agents: Sequence[int], layer_begin=None, layer_end=None, frame=0,
                       check=True):

@@ -223,8 +223,9 @@ def test_layer_subrange_and_agent_subset():
 
 
 def test_overlapped_round_matches_oracle():
-    """Selection and master on a second stream, overlapped with the re-rotation of the
-    other layers: the store and the restored pool are still the oracle's, bit for bit."""
+    """Selection, master and encode on a second stream, overlapped with the re-rotation of
+    the other layers: the store and the restored pool are still the oracle's, bit for
+    bit."""
     R = _R()
     cfg = synth.qwen7b().replace(n_layers=4, check_layer=2)
     ch = rk.run_oracle_chain(rk.make_inputs(cfg))
@@ -253,8 +254,8 @@ def test_overlapped_round_matches_oracle():
 
 
 def test_round_changes_on_a_shared_context_across_streams():
-    """Rounds A, B, A through one context, each with its selection and master on a side
-    stream overlapped with the re-rotation; B on streams of its own. Nothing synchronizes
+    """Rounds A, B, A through one context, each with its selection, master and encode on a
+    side stream overlapped with the re-rotation; B on streams of its own. Nothing synchronizes
     the host between them: the library must order each stream after the round's table
     upload and hold each upload until the work that reads the previous tables is done.
     Every round's outputs are the oracle's, bit for bit."""
