@@ -785,7 +785,7 @@ def report_chunked(args, cfg, seed, device, rank, world):
                          "frac": round(by[dom] / (stage_ms[dom] * 1e-3) / 1e9 / peak, 4),
                          "traffic": None, "peak_kind": peak_kind},
             "storage": storage_ratios(cfg, nnz, L),
-            "gpu_launches": args.steps * (3 + 5 * ((L + args.chunk_layers - 1) // args.chunk_layers)),
+            "gpu_launches": args.steps * (4 + 5 * ((L + args.chunk_layers - 1) // args.chunk_layers)),
             "clocks": clk.summary(),
             "e2e": None, "cpu_baseline": None,
         }
