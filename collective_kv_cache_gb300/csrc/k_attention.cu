@@ -26,8 +26,8 @@
 //     head), so rescaling needs no exchange;
 //   - the next stage's source rows are looked up before this stage's products, so the
 //     lookups' latency hides behind them;
-//   - the unit writes its partial (max, sum, unnormalised output); attn_combine_kernel
-//     merges an agent's units.
+//   - the unit writes its partial (max, sum, unnormalised output) of the G query heads;
+//     attn_combine_kernel merges an agent's units.
 // The same kernel with every position read from the pages (kFromPool) is plain paged
 // decode attention over a restored cache: the baseline the fusion replaces.
 #include "td_device.cuh"
@@ -362,20 +362,28 @@ attn_unit_kernel(const __grid_constant__ AttnArgs A, const __grid_constant__ Att
     l_part[c2] += __shfl_xor_sync(0xFFFFFFFFu, l_part[c2], 8);
     l_part[c2] += __shfl_xor_sync(0xFFFFFFFFu, l_part[c2], 16);
   }
+  // the partial of the group's G query heads only ([unit][G][D] and [unit][G][2])
   const int64_t unit = blockIdx.x;
-  float* po = A.part_o + unit * kAttnGMax * D;
+  float* po = A.part_o + unit * A.G * D;
+  const bool c0 = 2 * tig < A.G, c1 = 2 * tig + 1 < A.G;
 #pragma unroll
   for (int mt = 0; mt < KCH; ++mt) {
-    po[(2 * tig) * D + mt * 16 + gid] = oacc[mt][0];
-    po[(2 * tig + 1) * D + mt * 16 + gid] = oacc[mt][1];
-    po[(2 * tig) * D + mt * 16 + gid + 8] = oacc[mt][2];
-    po[(2 * tig + 1) * D + mt * 16 + gid + 8] = oacc[mt][3];
+    if (c0) {
+      po[(2 * tig) * D + mt * 16 + gid] = oacc[mt][0];
+      po[(2 * tig) * D + mt * 16 + gid + 8] = oacc[mt][2];
+    }
+    if (c1) {
+      po[(2 * tig + 1) * D + mt * 16 + gid] = oacc[mt][1];
+      po[(2 * tig + 1) * D + mt * 16 + gid + 8] = oacc[mt][3];
+    }
   }
   if (gid == 0) {
 #pragma unroll
     for (int c2 = 0; c2 < 2; ++c2) {
-      A.part_ml[(unit * kAttnGMax + 2 * tig + c2) * 2] = m_run[c2];
-      A.part_ml[(unit * kAttnGMax + 2 * tig + c2) * 2 + 1] = l_part[c2];
+      if (2 * tig + c2 < A.G) {
+        A.part_ml[(unit * A.G + 2 * tig + c2) * 2] = m_run[c2];
+        A.part_ml[(unit * A.G + 2 * tig + c2) * 2 + 1] = l_part[c2];
+      }
     }
   }
 }
@@ -404,7 +412,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs A, AttnList 
   float mx = -INFINITY;
   for (int i0 = 0; i0 < nu; i0 += 32) {
     const int i = i0 + lane;
-    if (i < nu) mx = fmaxf(mx, A.part_ml[(unit_of(i) * kAttnGMax + g) * 2]);
+    if (i < nu) mx = fmaxf(mx, A.part_ml[(unit_of(i) * A.G + g) * 2]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
@@ -416,15 +424,15 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs A, AttnList 
     float wgt = 0.0f;
     if (i < nu) {
       const int64_t unit = unit_of(i);
-      const float m = A.part_ml[(unit * kAttnGMax + g) * 2];
+      const float m = A.part_ml[(unit * A.G + g) * 2];
       wgt = m == -INFINITY ? 0.0f : exp2f(m - mx);
-      l = __fmaf_rn(A.part_ml[(unit * kAttnGMax + g) * 2 + 1], wgt, l);
+      l = __fmaf_rn(A.part_ml[(unit * A.G + g) * 2 + 1], wgt, l);
     }
     const int nb = min(32, nu - i0);
 #pragma unroll 8
     for (int j = 0; j < nb; ++j) {
       const float wj = __shfl_sync(0xFFFFFFFFu, wgt, j);
-      const float* po = A.part_o + (unit_of(i0 + j) * kAttnGMax + g) * D + lane * DPL;
+      const float* po = A.part_o + (unit_of(i0 + j) * A.G + g) * D + lane * DPL;
       if constexpr (DPL == 4) {
         const float4 q4 = *reinterpret_cast<const float4*>(po);
         acc[0] = __fmaf_rn(q4.x, wj, acc[0]);

@@ -156,8 +156,8 @@ struct AttnArgs {
   const uint16_t* q;         // [nl][n_list][nq][D] bf16
   float* out;                // [nl][n_list][nq][D]
   float* lse;                // [nl][n_list][nq] or nullptr
-  float* part_o;             // [units][kAttnGMax][D]
-  float* part_ml;            // [units][kAttnGMax][2]: max, sum (base 2)
+  float* part_o;             // [units][G][D]
+  float* part_ml;            // [units][G][2]: max, sum (base 2)
   int n_list, x0;            // the whole list's length; this launch's first entry
   int nq, G;                 // query heads, query heads per kv head
   int nl, layer_begin, sl0;  // layers; store layer of layer_begin
