@@ -22,7 +22,7 @@
 //                from the round's table, then the block table). The deviations go to
 //                `dev`; the first 12 bits of each key are counted in the agent's histogram.
 //   topk_kernel  one 512-thread CTA per agent: the histogram gives the threshold's first
-//                digit, two 10-bit passes over the agent's keys (held in registers)
+//                digit, two 10-bit passes over the agent's keys (staged in shared memory)
 //                give the rest, and warp ballots in token order write the selection
 //                ascending. It clears the histogram for the next call.
 #include "td_device.cuh"
@@ -33,6 +33,7 @@ namespace td {
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelBins2 = 1024;        // second and third digits: bits 19..10 and 9..0
+constexpr int kSelKeysSmem = 16384;    // keys an agent's selection stages (64 KiB)
 
 // Exclusive prefix over the CTA's kSelThreads threads in thread order; *total gets the sum.
 template <typename T>
@@ -94,49 +95,36 @@ __device__ __forceinline__ void find_digit(const uint32_t (&h)[kPer], int top, i
 }
 
 // The k largest of one agent's S keys (ties to the lower token), ascending, into out[0..k).
-// Warp w owns the tokens [w*cw, (w+1)*cw) (cw = S / kSelWarps rounded up to 32); lane l
-// holds the keys of tokens w*cw + 32j + l, j = 0, 1, ..., in registers when a warp's range
-// has at most 32 * kSelRegKeys tokens (else every pass reads them again through L2).
 // keys_g: the keys in global memory (written by other CTAs: read through L2). hist_g: their
 // first-digit histogram in global memory (read, then cleared), or nullptr to count it here
-// in s_h1 (kSelHistBins words). s_h: 2 * kSelBins2 words. Every thread of the CTA calls it.
-constexpr int kSelRegKeys = 32;
-
+// in s_h1 (kSelHistBins words). s_keys: kSelKeysSmem words of shared memory, or nullptr
+// (the keys are then read from L2 by every pass). s_h: 2 * kSelBins2 words. Every thread of
+// the CTA calls it.
 __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* hist_g,
-                             int32_t* __restrict__ out, uint32_t* s_h1, uint32_t* s_h) {
+                             int32_t* __restrict__ out, uint32_t* s_keys, uint32_t* s_h1,
+                             uint32_t* s_h) {
   __shared__ unsigned s_warp[kSelWarps];
   __shared__ unsigned long long s_warp64[kSelWarps];
   __shared__ int s_d1[3], s_d2[3], s_d3[3];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int cw = ((S + kSelWarps - 1) / kSelWarps + 31) & ~31;
-  const int w0 = min(S, wid * cw), w1 = min(S, w0 + cw);
-  const int nj = (w1 - w0 + 31) >> 5;            // groups of 32 tokens of this warp
-  const bool in_regs = cw <= 32 * kSelRegKeys;   // uniform across the CTA
-  uint32_t kr[kSelRegKeys];
-  if (in_regs) {                                 // every load issued before any is used
+  const bool staged = s_keys && S <= kSelKeysSmem;
+  if (staged) {
+    constexpr int kBatch = 4;                         // a thread's loads in flight together
+    for (int t0 = 0; t0 < S; t0 += kSelThreads * kBatch) {
+      uint32_t v[kBatch];
 #pragma unroll
-    for (int j = 0; j < kSelRegKeys; ++j) {
-      const int t = w0 + 32 * j + lane;
-      kr[j] = j < nj && t < w1 ? __ldcg(keys_g + t) : 0u;
+      for (int q = 0; q < kBatch; ++q) {
+        const int t = t0 + q * kSelThreads + tid;
+        v[q] = t < S ? __ldcg(keys_g + t) : 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int t = t0 + q * kSelThreads + tid;
+        if (t < S) s_keys[t] = v[q];
+      }
     }
   }
-  // fn(t, live, key) for the warp's groups in token order (uniform across the warp)
-  auto for_groups = [&](auto&& fn) {
-    if (in_regs) {
-#pragma unroll
-      for (int j = 0; j < kSelRegKeys; ++j) {
-        if (j < nj) {
-          const int t = w0 + 32 * j + lane;
-          fn(t, t < w1, kr[j]);
-        }
-      }
-    } else {
-      for (int j = 0; j < nj; ++j) {
-        const int t = w0 + 32 * j + lane;
-        fn(t, t < w1, t < w1 ? __ldcg(keys_g + t) : 0u);
-      }
-    }
-  };
+  auto key_at = [&](int t) { return staged ? s_keys[t] : __ldcg(keys_g + t); };
   constexpr int kPer1 = kSelHistBins / kSelThreads;   // 8
   uint32_t h1[kPer1];
   if (hist_g) {
@@ -152,15 +140,16 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
       h1[kPer1 - 3 - 4 * q] = v[q].z;
       h1[kPer1 - 4 - 4 * q] = v[q].w;
     }
+    __syncthreads();                                  // the staged keys
   } else {
     for (int b = tid; b < kSelHistBins; b += kSelThreads) s_h1[b] = 0u;
-    __syncthreads();
-    for_groups([&](int, bool live, uint32_t key) {   // one atomic per distinct bin of a warp
-      const unsigned d = live ? (key >> 20) : 0xFFFFFFFFu;
+    __syncthreads();                                  // the staged keys, the cleared bins
+    for (int t0 = 0; t0 < S; t0 += kSelThreads) {     // uniform trip count
+      const int t = t0 + tid;
+      const unsigned d = t < S ? (key_at(t) >> 20) : 0xFFFFFFFFu;
       const unsigned peers = __match_any_sync(0xFFFFFFFFu, d);
-      if (live && lane == __ffs(peers) - 1)
-        atomicAdd(&s_h1[d], static_cast<unsigned>(__popc(peers)));
-    });
+      if (t < S && lane == __ffs(peers) - 1) atomicAdd(&s_h1[d], static_cast<unsigned>(__popc(peers)));
+    }
     __syncthreads();
 #pragma unroll
     for (int q = 0; q < kPer1; ++q) h1[q] = s_h1[kSelHistBins - 1 - kPer1 * tid - q];
@@ -179,9 +168,10 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
   constexpr int kPer2 = kSelBins2 / kSelThreads;   // 2
   if (s_d1[1] != s_d1[2]) {
     // digit 2 (bits 19..10) among the keys of bin d1
-    for_groups([&](int, bool live, uint32_t key) {
-      if (live && (key >> 20) == d1) atomicAdd(&s_h2[(key >> 10) & 1023u], 1u);
-    });
+    for (int t = tid; t < S; t += kSelThreads) {
+      const uint32_t key = key_at(t);
+      if ((key >> 20) == d1) atomicAdd(&s_h2[(key >> 10) & 1023u], 1u);
+    }
     __syncthreads();
     uint32_t h2[kPer2];
 #pragma unroll
@@ -191,9 +181,10 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
     T = (static_cast<int64_t>(p2) << 10) - 1;
     if (s_d2[1] != s_d2[2]) {
       // digit 3 (bits 9..0) among the keys of bin (d1, d2)
-      for_groups([&](int, bool live, uint32_t key) {
-        if (live && (key >> 10) == p2) atomicAdd(&s_h3[key & 1023u], 1u);
-      });
+      for (int t = tid; t < S; t += kSelThreads) {
+        const uint32_t key = key_at(t);
+        if ((key >> 10) == p2) atomicAdd(&s_h3[key & 1023u], 1u);
+      }
       __syncthreads();
       uint32_t h3[kPer2];
 #pragma unroll
@@ -203,14 +194,17 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
       need_eq = s_d3[1];
     }
   }
-  // the output: each warp walks its tokens 32 at a time in token order; ballots of (above
-  // T) and (equal to T) give each taken token its place
+  // the output: warp w walks the tokens [w*cw, (w+1)*cw), 32 at a time in token order;
+  // ballots of (above T) and (equal to T) give each taken token its place
+  const int cw = ((S + kSelWarps - 1) / kSelWarps + 31) & ~31;
+  const int w0 = min(S, wid * cw), w1 = min(S, w0 + cw);
   unsigned n_gt = 0, n_eq = 0;
-  for_groups([&](int, bool live, uint32_t key) {
-    const int64_t kk = live ? static_cast<int64_t>(key) : -1;
+  for (int b = w0; b < w1; b += 32) {
+    const int t = b + lane;
+    const int64_t kk = t < w1 ? static_cast<int64_t>(key_at(t)) : -1;
     n_gt += __popc(__ballot_sync(0xFFFFFFFFu, kk > T));
     n_eq += __popc(__ballot_sync(0xFFFFFFFFu, kk == T));
-  });
+  }
   unsigned long long tot;
   const unsigned long long mine = (static_cast<unsigned long long>(n_gt) << 32) | n_eq;
   const unsigned long long excl =
@@ -219,8 +213,9 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
   int eq_seen = static_cast<int>(wex & 0xFFFFFFFFull);
   int pos = static_cast<int>(wex >> 32) + min(eq_seen, need_eq);
   const unsigned below = (1u << lane) - 1u;
-  for_groups([&](int t, bool live, uint32_t key) {
-    const int64_t kk = live ? static_cast<int64_t>(key) : -1;
+  for (int b = w0; b < w1; b += 32) {
+    const int t = b + lane;
+    const int64_t kk = t < w1 ? static_cast<int64_t>(key_at(t)) : -1;
     const unsigned gt = __ballot_sync(0xFFFFFFFFu, kk > T);
     const unsigned eq = __ballot_sync(0xFFFFFFFFu, kk == T);
     // the equal keys still wanted: the first need_eq - eq_seen of this group's
@@ -233,7 +228,7 @@ __device__ void select_agent(const uint32_t* keys_g, int S, int k, uint32_t* his
     }
     pos += __popc(taken);
     eq_seen += __popc(eq);
-  });
+  }
 }
 
 // ---- dev_kernel
@@ -448,17 +443,31 @@ topk_kernel(const float* __restrict__ dev, int S, int k, int32_t* __restrict__ s
             uint32_t* hist) {
   __shared__ uint32_t s_h1[kSelHistBins];
   __shared__ uint32_t s_h[2 * kSelBins2];
+  extern __shared__ uint32_t s_keys[];
   pdl_wait();
   const int i = blockIdx.x;
   select_agent(reinterpret_cast<const uint32_t*>(dev) + static_cast<int64_t>(i) * S, S, k,
                hist ? hist + static_cast<int64_t>(i) * kSelHistBins : nullptr,
-               sel + static_cast<int64_t>(i) * k, s_h1, s_h);
+               sel + static_cast<int64_t>(i) * k, S <= kSelKeysSmem ? s_keys : nullptr, s_h1,
+               s_h);
 }
 
 static cudaError_t launch_topk(const float* dev, int N, int S, int k, int32_t* sel,
                                uint32_t* hist, cudaStream_t st) {
   if (k <= 0 || N <= 0) return cudaSuccess;
-  return launch_after(topk_kernel, static_cast<unsigned>(N), kSelThreads, 0, st, dev, S, k,
+  static int opted[64] = {};
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  if (!opted[d]) {   // the staged keys pass the default shared-memory window
+    if ((e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSelKeysSmem * 4)) != cudaSuccess)
+      return e;
+    opted[d] = 1;
+  }
+  const size_t smem = static_cast<size_t>(S < kSelKeysSmem ? S : kSelKeysSmem) * 4;
+  return launch_after(topk_kernel, static_cast<unsigned>(N), kSelThreads, smem, st, dev, S, k,
                       sel, hist);
 }
 
