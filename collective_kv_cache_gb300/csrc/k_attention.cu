@@ -9,7 +9,8 @@
 // off_aj + u with K = R(off_aj) X; instead of turning every key the kernel turns the query
 // once per block, q . R(off) X = (R(-off) q) . X, so shared rows are used as stored.
 //
-// Work unit = (layer, kv head, agent, 512 positions of the agent's context), one warp:
+// Work unit = (layer, kv head, agent, 512 positions of the agent's context; 128 in the last
+// layers), one warp:
 //   - the rows of the head (D bf16 per position) are staged in shared memory by the TMA
 //     engine from 2-D tensor maps of the pool, the records and the Master (16 x 64 boxes,
 //     128-byte swizzle): a stage is at most 16 positions from one page, one diff block and
@@ -27,7 +28,10 @@
 //   - the next stage's source rows are looked up before this stage's products, so the
 //     lookups' latency hides behind them;
 //   - the unit writes its partial (max, sum, unnormalised output) of the G query heads;
-//     attn_combine_kernel merges an agent's units.
+//     attn_combine_kernel merges an agent's units;
+//   - the grid ends with the last layers cut into 128-position units, so that the last
+//     units to start are short and the SMs stay busy until close to the end (in 512-position
+//     units the final wave left half the SMs idle for the last ~40 us).
 // The same kernel with every position read from the pages (kFromPool) is plain paged
 // decode attention over a restored cache: the baseline the fusion replaces.
 #include "td_device.cuh"
@@ -95,28 +99,33 @@ attn_unit_kernel(const __grid_constant__ AttnArgs A, const __grid_constant__ Att
 
   const int lane = threadIdx.x;
   const int gid = lane >> 2, tig = lane & 3;   // mma fragment group / thread in group
-  const int total = list.base[list.n];
-  int64_t u = blockIdx.x;
+  // the unit: layers [0, split) in long units first, then the rest in short ones
+  const int64_t n_long = static_cast<int64_t>(list.split) * A.g.H * list.base[list.n];
+  const bool short_unit = static_cast<int64_t>(blockIdx.x) >= n_long;
+  const int32_t* base = short_unit ? list.base2 : list.base;
+  const int ch = short_unit ? kAttnTailChunk : kAttnChunk;
+  const int total = base[list.n];
+  int64_t u = short_unit ? blockIdx.x - n_long : blockIdx.x;
   const int c = static_cast<int>(u % total);
   u /= total;
   const int h = static_cast<int>(u % A.g.H);
-  const int li = static_cast<int>(u / A.g.H);
+  const int li = static_cast<int>(u / A.g.H) + (short_unit ? list.split : 0);
   int lo = 0, hi = list.n - 1;                 // the agent of unit c
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (list.base[mid] <= c) lo = mid;
+    if (base[mid] <= c) lo = mid;
     else hi = mid - 1;
   }
   const int x = lo, a = list.a[x];
   const int S = A.rd.S, P = A.pool.P;
   const int n_ctx = list.hist[x] + S;
   const int hist = kFromPool ? n_ctx : list.hist[x];   // positions read from the pages
-  // units of an agent: its history in 512-position chunks, then its shared tokens in
-  // 512-token chunks (so no unit straddles the two and every stage starts aligned)
-  const int nh = (hist + kAttnChunk - 1) / kAttnChunk;
-  const int cu = c - list.base[x];
-  const int p0 = cu < nh ? cu * kAttnChunk : hist + (cu - nh) * kAttnChunk;
-  const int p1 = cu < nh ? min(p0 + kAttnChunk, hist) : min(p0 + kAttnChunk, n_ctx);
+  // units of an agent: its history in chunks of ch positions, then its shared tokens in
+  // chunks of ch tokens (so no unit straddles the two and every stage starts aligned)
+  const int nh = (hist + ch - 1) / ch;
+  const int cu = c - base[x];
+  const int p0 = cu < nh ? cu * ch : hist + (cu - nh) * ch;
+  const int p1 = cu < nh ? min(p0 + ch, hist) : min(p0 + ch, n_ctx);
   const int layer = A.layer_begin + li, sl = A.sl0 + li;
 
   if (lane < kAttnDepth) mbar_init(&s_bar[lane], 1);
@@ -402,10 +411,16 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs A, AttnList 
   const int x = static_cast<int>((w / A.nq) % list.n);
   const int li = static_cast<int>(w / (static_cast<int64_t>(A.nq) * list.n));
   const int h = gq / A.G, g = gq - h * A.G;
-  // the agent's units: contiguous from list.base[x] within (layer, kv head)
-  const int total = list.base[list.n];
-  const int64_t u0 = (static_cast<int64_t>(li) * A.g.H + h) * total + list.base[x];
-  const int nu = list.base[x + 1] - list.base[x];
+  // the agent's units: contiguous within (layer, kv head), long units before the split
+  // layer, short ones from it on (after all the long units of the launch)
+  const bool short_unit = li >= list.split;
+  const int32_t* base = short_unit ? list.base2 : list.base;
+  const int total = base[list.n];
+  const int64_t first = short_unit ? static_cast<int64_t>(list.split) * A.g.H * list.base[list.n]
+                                   : 0;
+  const int lr = short_unit ? li - list.split : li;
+  const int64_t u0 = first + (static_cast<int64_t>(lr) * A.g.H + h) * total + base[x];
+  const int nu = base[x + 1] - base[x];
   auto unit_of = [&](int i) { return u0 + i; };
   // the units' maxima and sums a lane per unit (batches of 32), so that their loads are in
   // flight together; then the weighted outputs, eight units' loads at a time
@@ -458,7 +473,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs A, AttnList 
 template <int D, bool kFromPool>
 static cudaError_t run_attn(const AttnArgs& a, const AttnList& list, const AttnMaps& maps,
                             cudaStream_t st) {
-  const int64_t units = static_cast<int64_t>(a.nl) * a.g.H * list.base[list.n];
+  const int64_t units = static_cast<int64_t>(list.split) * a.g.H * list.base[list.n] +
+                        static_cast<int64_t>(a.nl - list.split) * a.g.H * list.base2[list.n];
   if (units == 0) return cudaSuccess;
   cudaError_t e = launch_after(attn_unit_kernel<D, kFromPool>, static_cast<unsigned>(units), 32,
                                0, st, a, list, maps);

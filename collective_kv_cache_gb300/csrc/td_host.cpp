@@ -62,6 +62,7 @@ struct td_ctx {
   int32_t* d_wprefix = nullptr;     // [max_agents * nbw_max + max_agents]
   int64_t* d_aprefix = nullptr;     // [max_agents + 1]
   uint32_t* d_flag = nullptr;       // [max_agents * L * max_nb] flags + [max_agents * L] counts
+  int sm_count = 0;                 // of the context's device
   int32_t* d_ints = nullptr;        // encode's words (unused, m_ok, over, prep_done), spare,
                                     // pick_master's counter, spare
   int64_t* d_bound = nullptr;
@@ -429,18 +430,38 @@ td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store
   a.scale_log2 = scale * 1.4426950408889634f;
   a.tx_pad = c->attn_tx_pad;
   a.err = c->d_err;
-  // partials of the largest launch; grown once, after the work that used them
-  // an agent's units: its history, then its shared tokens, each in chunks of kAttnChunk
-  // (every position from the pages: the whole context in chunks)
-  auto units_of = [&](int x) -> int64_t {
+  // an agent's units: its history, then its shared tokens, each in chunks of `ch`
+  // positions (every position from the pages: the whole context in chunks)
+  auto units_of = [&](int x, int ch) -> int64_t {
     const int64_t hl = r->hist_len[agents[x]];
-    if (!store) return (hl + c->S + kAttnChunk - 1) / kAttnChunk;
-    return (hl + kAttnChunk - 1) / kAttnChunk + (c->S + kAttnChunk - 1) / kAttnChunk;
+    if (!store) return (hl + c->S + ch - 1) / ch;
+    return (hl + ch - 1) / ch + (c->S + ch - 1) / ch;
   };
+  // The grid ends with the last layers in short units, about half a wave of the machine
+  // (13 warps an SM, each on kAttnChunk positions), so that the last units to start are
+  // short. Only where a layer is less than half a wave: in larger rounds the final wave is
+  // a small part of the call, and a whole layer in short units would cost more partials
+  // than its tail saves.
+  const int nl = layer_end - layer_begin;
+  int n_short = 0;
+  {
+    int64_t per_layer = 0;   // context positions of one layer of the first agent list
+    for (int x = 0; x < n_list && x < kMaxListAgents; ++x)
+      per_layer += static_cast<int64_t>(r->hist_len[agents[x]]) + c->S;
+    per_layer *= H;
+    const int64_t half_wave = static_cast<int64_t>(c->sm_count) * 13 * kAttnChunk / 2;
+    if (per_layer > 0 && per_layer <= half_wave) {
+      const int64_t t = (half_wave + per_layer - 1) / per_layer;
+      n_short = static_cast<int>(t > nl - 1 ? nl - 1 : t);
+    }
+  }
+  const int split = nl - n_short;
+  // partials of the largest agent list; grown once, after the work that used them
   int64_t most = 0;
   for (int x0 = 0; x0 < n_list; x0 += kMaxListAgents) {
     int64_t sum = 0;
-    for (int x = x0; x < n_list && x < x0 + kMaxListAgents; ++x) sum += units_of(x);
+    for (int x = x0; x < n_list && x < x0 + kMaxListAgents; ++x)
+      sum += units_of(x, kAttnChunk) * split + units_of(x, kAttnTailChunk) * n_short;
     most = sum > most ? sum : most;
   }
   AttnMaps maps;
@@ -462,7 +483,7 @@ td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store
   } else {
     maps.master_k = maps.master_v = maps.val_k = maps.val_v = maps.pool;
   }
-  const size_t need = static_cast<size_t>(most) * a.nl * H * kAttnGMax * (D + 2);
+  const size_t need = static_cast<size_t>(most) * H * kAttnGMax * (D + 2);
   if (need > c->attn_cap) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return TD_ERR_CUDA;
     cudaFree(c->d_attn);
@@ -474,15 +495,19 @@ td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store
   for (int x0 = 0; x0 < n_list; x0 += kMaxListAgents) {
     AttnList L;
     L.n = n_list - x0 < kMaxListAgents ? n_list - x0 : kMaxListAgents;
-    L.base[0] = 0;
+    L.split = split;
+    L.base[0] = L.base2[0] = 0;
     for (int x = 0; x < L.n; ++x) {
       L.a[x] = agents[x0 + x];
       L.hist[x] = r->hist_len[agents[x0 + x]];
-      const int64_t nb = L.base[x] + units_of(x0 + x);
-      if (nb > INT32_MAX) return TD_ERR_INVALID_ARG;
+      const int64_t nb = L.base[x] + units_of(x0 + x, kAttnChunk);
+      const int64_t nb2 = L.base2[x] + units_of(x0 + x, kAttnTailChunk);
+      if (nb > INT32_MAX || nb2 > INT32_MAX) return TD_ERR_INVALID_ARG;
       L.base[x + 1] = static_cast<int32_t>(nb);
+      L.base2[x + 1] = static_cast<int32_t>(nb2);
     }
-    const int64_t units = static_cast<int64_t>(L.base[L.n]) * a.nl * H;
+    const int64_t units = static_cast<int64_t>(L.base[L.n]) * split * H +
+                          static_cast<int64_t>(L.base2[L.n]) * n_short * H;
     if (units > INT32_MAX) return TD_ERR_INVALID_ARG;
     a.x0 = x0;
     a.part_o = c->d_attn;
@@ -543,7 +568,9 @@ td_status td_ctx_create(const td_shape* shape, int32_t max_agents, int32_t max_b
   c->max_shared = max_shared;
   c->max_nb = max_nb;
   c->nbw_max = nbw;
-  if (cudaGetDevice(&c->device) != cudaSuccess) {
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device) !=
+          cudaSuccess) {
     delete c;
     return TD_ERR_CUDA;
   }

@@ -137,15 +137,21 @@ cudaError_t launch_restore(const Geom& g, const RoundDev& rd, const PoolDev& poo
 
 // Decode attention from the Master and the diffs (k_attention.cu).
 constexpr int kAttnChunk = 512;    // context positions per work unit (one warp)
+constexpr int kAttnTailChunk = 128; // ... in the units of the last layers (the grid's end)
 constexpr int kAttnStage = 16;     // positions per pipeline stage
 constexpr int kAttnDepth = 2;      // stages in flight per unit
 constexpr int kAttnGMax = 8;       // query heads per kv head
 
+// The units of a launch: layers [0, split) in units of kAttnChunk positions, then layers
+// [split, nl) in units of kAttnTailChunk, so that the grid ends with short units and the
+// SMs run full until close to the end.
 struct AttnList {
   int n;                               // agents of this launch
+  int split;                           // first layer (within the launch) of short units
   int32_t a[kMaxListAgents];           // their ids
   int32_t hist[kMaxListAgents];        // their history lengths
   int32_t base[kMaxListAgents + 1];    // exclusive prefix of their units (per layer, head)
+  int32_t base2[kMaxListAgents + 1];   // the same in short units
 };
 
 struct AttnArgs {
