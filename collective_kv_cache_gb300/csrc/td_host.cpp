@@ -439,18 +439,24 @@ td_status run_attention(td_ctx* c, const td_round* r, const td_diff_store* store
   };
   // The grid ends with the last layers in short units, about half a wave of the machine
   // (13 warps an SM, each on kAttnChunk positions), so that the last units to start are
-  // short. Only where a layer is less than half a wave: in larger rounds the final wave is
-  // a small part of the call, and a whole layer in short units would cost more partials
-  // than its tail saves.
+  // short. Only where a layer is less than half a wave and the grid is more than one wave:
+  // in larger layers the final wave is a small part of the call, and a whole layer in short
+  // units would cost more partials than its tail saves; a grid of one wave or less has no
+  // last wave to shorten, only more partials to combine.
   const int nl = layer_end - layer_begin;
   int n_short = 0;
   {
     int64_t per_layer = 0;   // context positions of one layer of the first agent list
-    for (int x = 0; x < n_list && x < kMaxListAgents; ++x)
+    int64_t long_units = 0;  // its units of kAttnChunk positions
+    for (int x = 0; x < n_list && x < kMaxListAgents; ++x) {
       per_layer += static_cast<int64_t>(r->hist_len[agents[x]]) + c->S;
+      long_units += units_of(x, kAttnChunk);
+    }
     per_layer *= H;
-    const int64_t half_wave = static_cast<int64_t>(c->sm_count) * 13 * kAttnChunk / 2;
-    if (per_layer > 0 && per_layer <= half_wave) {
+    long_units *= static_cast<int64_t>(H) * nl;
+    const int64_t wave = static_cast<int64_t>(c->sm_count) * 13;
+    const int64_t half_wave = wave * kAttnChunk / 2;
+    if (per_layer > 0 && per_layer <= half_wave && long_units > wave) {
       const int64_t t = (half_wave + per_layer - 1) / per_layer;
       n_short = static_cast<int>(t > nl - 1 ? nl - 1 : t);
     }

@@ -57,6 +57,12 @@ CASES = {
     "mini_p24": (_mini(page_size=24, hist_range=(30, 100), seed=115), 6),
     "mini_p8_d128": (_mini(page_size=8, head_dim=128, hist_range=(30, 100), seed=116), 4),
     "qwen7b_2layers": (synth.qwen7b().replace(n_layers=2), 28),
+    # more than one wave of 512-position units on a 152-SM GPU (13 a SM) while a layer is
+    # under half a wave: the grid ends with the last 4 of the 8 layers in 128-position units
+    "wide_p24": (_mini(n_agents=16, n_layers=8, page_size=24, hist_range=(3000, 5000),
+                       seed=117), 6),
+    "wide_b32_p32": (_mini(n_agents=16, n_layers=8, diff_block=32, page_size=32,
+                           hist_range=(3000, 5000), seed=118), 6),
 }
 
 
@@ -173,7 +179,7 @@ def test_fused_attention_matches_oracle(name):
 
 
 @pytest.mark.parametrize("name", ["mini_gqa3", "mini_d128_gqa2", "mini_long_history",
-                                  "qwen7b_2layers"])
+                                  "qwen7b_2layers", "wide_p24"])
 def test_paged_attention_matches_oracle(name):
     _run(name, paged=True)
 
